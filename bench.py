@@ -1,0 +1,457 @@
+#!/usr/bin/env python
+"""Benchmark of DDTree verify attention (MLA, absorbed form) on GB300.
+
+One step = one mla_verify_attn call (metadata kernel, split-KV attention,
+LSE combine) over the 200k-prefix workload: B=1, H=64, a 64-node draft tree
+(depth <= 8), 200,000 prefix tokens at scattered page_size=1 slots of a
+262,144-slot bf16 latent pool.  Inputs are seeded synthetic data of that shape.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU float64
+oracle instead, on bounded row samples of the same workload.
+
+Multi-GPU: the call has no exchange step, so N GPUs run N independent
+replicas of the workload (one process per GPU under torchrun); the timed
+region is bracketed by a barrier and the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mla_tree_verify_absorbed_gb300 import inputs as I  # noqa: E402
+
+METRIC = "verify-attn µs/call & effective KV GB/s (% HBM roofline), H=64, 200k prefix"
+UNIT = "us/call"
+WORKLOAD = "c3"
+WORKLOAD_DESC = ("B=1 H=64 prefix=200000 tree=64 nodes (depth<=8) Dl=512 Dr=64 bf16 "
+                 "page_size=1 slots = seeded permutation of a 262144-slot pool")
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+KERNELS_PER_CALL = 4  # metadata (2), attention, combine
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ----------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float, device="cpu") -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# workload arithmetic (counts for the roofline; not the method)
+# ----------------------------------------------------------------------------
+def workload_counts(p: I.Problem):
+    n = p.kv_lens.astype(np.float64)
+    rows = p.H * p.Q
+    el = 2 if p.dtype == "bf16" else 4
+    flops = float(2.0 * rows * n.sum() * (I.DL + I.DR + I.DL))   # 2 * rows * N * 1088
+    kv_bytes = float(n.sum() * I.DK * el)
+    q_bytes = float(p.B * rows * I.DK * el)
+    o_bytes = float(p.B * rows * (I.DL * el + 4))
+    idx_bytes = float(n.sum() * 4 + (p.B + 1) * 4 + p.B * 4 + p.B * p.Q * 4)
+    return dict(flops=flops, kv_bytes=kv_bytes, q_bytes=q_bytes, o_bytes=o_bytes, idx_bytes=idx_bytes)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as fh:
+                return json.load(fh), "measured"
+        except Exception:
+            pass
+    return None, "fallback"
+
+
+def peak_bf16_tflops():
+    pk, src = measured_peaks()
+    if pk:
+        for k in ("bf16_tflops", "bf16_tflops_burst", "bf16_dense_tflops"):
+            if k in pk and pk[k]:
+                return float(pk[k]), src
+    return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def peak_hbm_gbs():
+    pk, src = measured_peaks()
+    if pk:
+        for k in ("hbm_gbs", "hbm_copy_gbs"):
+            if k in pk and pk[k]:
+                return float(pk[k]), src
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_record(kernel_src: str):
+    """DRAM bytes per launch of the timed kernel from the committed ncu summary,
+    or None when that summary was taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path))
+        src = open(os.path.join(ROOT, "mla_tree_verify_absorbed_gb300", "csrc", kernel_src), "rb").read()
+        if rec.get("source_sha256") != hashlib.sha256(src).hexdigest():
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index=None):
+        self.proc = None
+        self.gpu_index = gpu_index
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.gpu_index is not None:
+            cmd += ["-i", str(self.gpu_index)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in csv.reader(io.StringIO(out)):
+            if len(row) < 9:
+                continue
+            try:
+                sm.append(float(row[1]))
+                smax.append(float(row[2]))
+            except ValueError:
+                continue
+            n += 1
+            for name, v in zip(names, row[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+def physical_gpu_index(local_rank: int):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        parts = [x.strip() for x in vis.split(",") if x.strip()]
+        if local_rank < len(parts) and parts[local_rank].isdigit():
+            return int(parts[local_rank])
+        return None
+    return local_rank
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and the reference arm)
+# ----------------------------------------------------------------------------
+def time_oracle_rows(p: I.Problem, n_rows: int, seed: int):
+    import oracle
+    orc = oracle.get()
+    rows_all = I.sample_rows(p, p.H, seed=seed)
+    rng = np.random.default_rng(seed)
+    rows = rows_all[rng.choice(len(rows_all), size=min(n_rows, len(rows_all)), replace=False)]
+    t0 = time.perf_counter()
+    orc.verify_rows(p, rows)
+    dt = time.perf_counter() - t0
+    return dt, len(rows), orc.num_threads()
+
+
+def cpu_baseline(p: I.Problem, target_s: float = 12.0):
+    """Oracle on a bounded row sample, scaled to microseconds per full call."""
+    import oracle
+    cores = oracle.get().num_threads()
+    dt, n, _ = time_oracle_rows(p, cores, seed=101)            # calibrate: one row per thread
+    per_row = dt / max(n, 1)
+    n2 = int(min(max(cores, target_s / max(per_row, 1e-6) * 0.9), 4 * cores * 8))
+    n2 = max(cores, (n2 // cores) * cores)
+    dt2, n2, cores = time_oracle_rows(p, n2, seed=102)
+    total_rows = p.B * p.H * p.Q
+    us_call = dt2 / n2 * total_rows * 1e6
+    return {"value": us_call, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n2} of {total_rows} query rows (seeded), {dt2:.2f} s wall; "
+                      f"value = measured time per row x all rows"}
+
+
+# ----------------------------------------------------------------------------
+# arms
+# ----------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    p = I.make_config(args.workload)
+    cores = oracle.get().num_threads()
+    for w in range(args.warmup):
+        time_oracle_rows(p, cores, seed=1000 + w)
+    times, nrows = [], 0
+    for k in range(args.steps):
+        dt, n, cores = time_oracle_rows(p, cores, seed=2000 + k)
+        times.append(dt / n)
+        nrows += n
+    total_rows = p.B * p.H * p.Q
+    us_call = float(np.mean(times)) * total_rows * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us_call, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": us_call / 1000.0,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": f"{args.workload}: {WORKLOAD_DESC}"},
+        "cpu_baseline": {"value": us_call, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} steps x {cores} seeded query rows of "
+                                   f"{total_rows}; value = mean time per row x all rows"},
+        "e2e": {"value": us_call, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    from mla_tree_verify_absorbed_gb300 import api
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    api.load()
+
+    p = I.make_config(args.workload)
+    cnt = workload_counts(p)
+    di = api.device_inputs(p, device=dev)
+    algo = args.algo
+    stream = torch.cuda.current_stream(dev)
+    out = torch.empty((p.B, p.Q, p.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((p.B, p.Q, p.H), dtype=torch.float32, device=dev)
+    ws = api.alloc_workspace(api.workspace_size(di, args.num_splits, algo), dev)
+
+    for _ in range(args.warmup):
+        api.verify_attn(di, out=out, lse=lse, num_splits=args.num_splits, algo=algo, workspace=ws)
+    torch.cuda.synchronize(dev)
+    bits = api.check(ws)
+    if bits:
+        raise SystemExit(f"device table check failed: {bits:#x}")
+
+    # --- device-resident timed region ---------------------------------------
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(physical_gpu_index(local)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for k in range(args.steps):
+        api.verify_attn(di, out=out, lse=lse, num_splits=args.num_splits, algo=algo, workspace=ws,
+                        profile_events=evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    clocks = sampler.stop() if sampler else None
+    elapsed_ms = t_start.elapsed_time(t_end)
+    attn_ms = [a.elapsed_time(b) for a, b in evs]
+    elapsed_ms = max_over_ranks(dist, elapsed_ms, device=dev)
+    attn_avg_ms = max_over_ranks(dist, float(np.mean(attn_ms)), device=dev)
+
+    # --- end to end through the public API with host buffers ----------------
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, p, di, dev, stream, algo, dist)
+
+    if rank != 0:
+        return 0
+
+    ms_step = elapsed_ms / args.steps
+    us_call = ms_step * 1000.0 / world
+    kernel_s = attn_avg_ms / 1000.0
+    eff_kv_gbs = cnt["kv_bytes"] / (ms_step / 1000.0) / 1e9
+    resolved = "tc" if (algo == "tc" or (algo == "auto" and tc_is_default())) else "simt"
+    if resolved == "tc":
+        peak, src = peak_bf16_tflops()
+        achieved = cnt["flops"] / kernel_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic_record("attn_tc.cu"),
+                "peak_source": f"bf16 dense, {src}", "kernel": "attn_tc_kernel",
+                "kernel_us": attn_avg_ms * 1000.0}
+    else:
+        sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = (clocks or {}).get("sm_max_mhz") or 2070.0
+        peak = sm * 128 * 2 * mhz * 1e6 / 1e12
+        achieved = cnt["flops"] / kernel_s / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic_record("attn_simt.cu"),
+                "peak_source": f"fp32 FFMA: {sm} SMs x 128 lanes x 2 x {mhz:.0f} MHz",
+                "kernel": "attn_simt_kernel", "kernel_us": attn_avg_ms * 1000.0}
+    hbm_peak, hsrc = peak_hbm_gbs()
+    hbm_bytes = cnt["kv_bytes"] + cnt["q_bytes"] + cnt["o_bytes"]
+    t_roof = max(hbm_bytes / (hbm_peak * 1e9), cnt["flops"] / (peak_bf16_tflops()[0] * 1e12))
+
+    line = {
+        "metric": METRIC, "value": us_call, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {WORKLOAD_DESC}", "algo": resolved,
+                   "num_splits": args.num_splits,
+                   "l2": "inputs larger than L2: 230 MB of KV read per call (129 MB L2)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "effective_kv_gbs": eff_kv_gbs,
+        "tflops": cnt["flops"] / (ms_step / 1000.0) / 1e12,
+        "roofline_fraction_of_call": t_roof / (ms_step / 1000.0),
+        "hbm_fraction": (hbm_bytes / (ms_step / 1000.0) / 1e9) / hbm_peak,
+        "hbm_peak_source": hsrc,
+        "roofline": roof,
+        "gpu_launches": KERNELS_PER_CALL * args.steps,
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(p)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def tc_is_default() -> bool:
+    """Whether AUTO picks the tensor-core kernel for bf16 (asks the library)."""
+    import ctypes
+    from mla_tree_verify_absorbed_gb300 import api
+    a = api.MlaVerifyArgs()
+    a.B, a.Q, a.H, a.dtype = 1, 1, 128, api.MLA_BF16
+    p = 0x10000
+    for f in ("q_lat", "q_pe", "kv_c", "k_pe", "kv_indptr", "kv_indices", "prefix_lens",
+              "tree_parent", "out"):
+        setattr(a, f, p)
+        p += 0x10000
+    a.kv_c_stride, a.k_pe_stride, a.pool_slots, a.page_size, a.scale = 576, 576, 16, 1, 0.1
+    a.algo = api.ALGO["auto"]
+    n_auto = api.load().mla_verify_workspace_size(ctypes.byref(a), 1)
+    a.algo = api.ALGO["tc"]
+    n_tc = api.load().mla_verify_workspace_size(ctypes.byref(a), 1)
+    return n_auto == n_tc
+
+
+def run_e2e(args, p, di, dev, stream, algo, dist):
+    """Per step: H2D of the step's queries, tree and index tables from pinned
+    host memory, the C-ABI call, D2H of out and lse.  The KV pool is the cache:
+    resident on the device, not copied per step."""
+    import torch
+    from mla_tree_verify_absorbed_gb300 import api
+
+    host = {}
+    for name in ("q_lat", "q_pe", "prefix_lens", "tree_parent", "kv_indptr", "kv_indices", "block_table"):
+        t = getattr(di, name)
+        if t is not None:
+            host[name] = t.cpu().pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    out_h = torch.empty((p.B, p.Q, p.H, 512), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((p.B, p.Q, p.H), dtype=torch.float32).pin_memory()
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    out = torch.empty((p.B, p.Q, p.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((p.B, p.Q, p.H), dtype=torch.float32, device=dev)
+    ws = api.alloc_workspace(api.workspace_size(di, args.num_splits, algo), dev)
+
+    def step():
+        for name, h in host.items():
+            getattr(di, name).copy_(h, non_blocking=True)
+        api.verify_attn(di, out=out, lse=lse, num_splits=args.num_splits, algo=algo, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    ms = max_over_ranks(dist, a.elapsed_time(b), device=dev)
+    world = dist.get_world_size() if dist is not None else 1
+    return {"value": ms * 1000.0 / args.steps / world, "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD, choices=list(I.CONFIG_NAMES))
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--algo", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3  # timing rule: at least three untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,251 @@
+"""ctypes binding of the C ABI in include/mla_verify.h.
+
+Argument marshalling only: torch tensors give device pointers, sizes and
+strides; every step of the computation runs in the CUDA library.  The library
+is loaded on first use and a missing build raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libmla_verify.so")
+
+MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA, MLA_ERR_WORKSPACE, \
+    MLA_ERR_DEVICE_CHECK = range(6)
+MLA_BF16, MLA_FP32 = 0, 1
+ALGO = {"auto": 0, "simt": 1, "tc": 2}
+
+DEVERR = {
+    0x1: "PREFIX", 0x2: "INDPTR", 0x4: "SLOT", 0x8: "PARENT", 0x10: "PAGES",
+    0x20: "CAPACITY", 0x40: "TIMEOUT",
+}
+
+# every symbol include/mla_verify.h declares
+EXPORTS = ("mla_verify_workspace_size", "mla_verify_attn", "mla_verify_build_meta",
+           "mla_verify_check", "mla_status_str", "mla_verify_abi_version")
+
+
+class MlaVerifyArgs(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int), ("Q", ctypes.c_int), ("H", ctypes.c_int),
+        ("dtype", ctypes.c_int),
+        ("q_lat", ctypes.c_void_p), ("q_pe", ctypes.c_void_p),
+        ("kv_c", ctypes.c_void_p), ("k_pe", ctypes.c_void_p),
+        ("kv_c_stride", ctypes.c_int64), ("k_pe_stride", ctypes.c_int64),
+        ("pool_slots", ctypes.c_int64),
+        ("page_size", ctypes.c_int),
+        ("kv_indptr", ctypes.c_void_p), ("kv_indices", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p), ("max_pages", ctypes.c_int),
+        ("prefix_lens", ctypes.c_void_p), ("tree_parent", ctypes.c_void_p),
+        ("scale", ctypes.c_float),
+        ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("algo", ctypes.c_int),
+        ("profile_events", ctypes.c_void_p),
+    ]
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_str(status)}")
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None):
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library not built: {p} (run __graft_entry__.build())")
+    lib = ctypes.CDLL(p)
+    lib.mla_verify_workspace_size.restype = ctypes.c_size_t
+    lib.mla_verify_workspace_size.argtypes = [ctypes.POINTER(MlaVerifyArgs), ctypes.c_int]
+    lib.mla_verify_attn.restype = ctypes.c_int
+    lib.mla_verify_attn.argtypes = [ctypes.POINTER(MlaVerifyArgs), ctypes.c_void_p, ctypes.c_size_t,
+                                    ctypes.c_int, ctypes.c_void_p]
+    lib.mla_verify_build_meta.restype = ctypes.c_int
+    lib.mla_verify_build_meta.argtypes = [ctypes.POINTER(MlaVerifyArgs), ctypes.c_void_p, ctypes.c_size_t,
+                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                          ctypes.c_void_p]
+    lib.mla_verify_check.restype = ctypes.c_int
+    lib.mla_verify_check.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
+    lib.mla_status_str.restype = ctypes.c_char_p
+    lib.mla_status_str.argtypes = [ctypes.c_int]
+    lib.mla_verify_abi_version.restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_str(s: int) -> str:
+    return load().mla_status_str(int(s)).decode()
+
+
+# ----------------------------------------------------------------------------
+# torch marshalling
+# ----------------------------------------------------------------------------
+def _ptr(t) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+@dataclass
+class DeviceInputs:
+    """Device tensors of one verify problem (see inputs.Problem)."""
+    B: int
+    Q: int
+    H: int
+    dtype: str
+    scale: float
+    q_lat: object
+    q_pe: object
+    kv_c: object            # [pool_slots, >=512] view (row stride = pool row)
+    k_pe: object            # [pool_slots, >=64] view
+    prefix_lens: object
+    tree_parent: object
+    page_size: int
+    kv_indptr: object = None
+    kv_indices: object = None
+    block_table: object = None
+    pool: object = None     # owning tensor of kv_c / k_pe
+
+    @property
+    def pool_slots(self) -> int:
+        return int(self.kv_c.shape[0])
+
+
+def device_inputs(problem, device="cuda", separate_pools: bool = False) -> DeviceInputs:
+    """Copy a numpy inputs.Problem to the device (packed [slot][576] pool by
+    default; separate kv_c / k_pe arrays with ``separate_pools``)."""
+    import torch
+
+    def t(x, dt=None):
+        if x is None:
+            return None
+        a = np.ascontiguousarray(x)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+        tt = torch.from_numpy(a).to(device)
+        return tt if dt is None else tt.to(dt)
+
+    pool = t(problem.pool)
+    if separate_pools:
+        kv_c = pool[:, :512].contiguous()
+        k_pe = pool[:, 512:].contiguous()
+        owner = None
+    else:
+        kv_c, k_pe, owner = pool[:, :512], pool[:, 512:], pool
+    return DeviceInputs(
+        B=problem.B, Q=problem.Q, H=problem.H, dtype=problem.dtype, scale=problem.scale,
+        q_lat=t(problem.q_lat), q_pe=t(problem.q_pe), kv_c=kv_c, k_pe=k_pe,
+        prefix_lens=t(problem.prefix_lens.astype(np.int32)),
+        tree_parent=t(problem.tree_parent.astype(np.int32)),
+        page_size=problem.page_size,
+        kv_indptr=t(problem.kv_indptr), kv_indices=t(problem.kv_indices),
+        block_table=t(problem.block_table), pool=owner)
+
+
+def make_args(di: DeviceInputs, out=None, lse=None, algo: str = "auto",
+              profile_events=None) -> MlaVerifyArgs:
+    a = MlaVerifyArgs()
+    a.B, a.Q, a.H = di.B, di.Q, di.H
+    a.dtype = MLA_BF16 if di.dtype == "bf16" else MLA_FP32
+    a.q_lat, a.q_pe = _ptr(di.q_lat), _ptr(di.q_pe)
+    a.kv_c, a.k_pe = _ptr(di.kv_c), _ptr(di.k_pe)
+    a.kv_c_stride = int(di.kv_c.stride(0))
+    a.k_pe_stride = int(di.k_pe.stride(0))
+    a.pool_slots = di.pool_slots
+    a.page_size = di.page_size
+    a.kv_indptr, a.kv_indices = _ptr(di.kv_indptr), _ptr(di.kv_indices)
+    a.block_table = _ptr(di.block_table)
+    a.max_pages = 0 if di.block_table is None else int(di.block_table.shape[1])
+    a.prefix_lens, a.tree_parent = _ptr(di.prefix_lens), _ptr(di.tree_parent)
+    a.scale = di.scale
+    a.out, a.lse = _ptr(out), _ptr(lse)
+    a.algo = ALGO[algo]
+    if profile_events is not None:
+        # keep the pointer array alive as long as the struct
+        a._ev = (ctypes.c_void_p * 2)(int(profile_events[0].cuda_event), int(profile_events[1].cuda_event))
+        a.profile_events = ctypes.cast(a._ev, ctypes.c_void_p)
+    return a
+
+
+def workspace_size(di: DeviceInputs, num_splits: int = 0, algo: str = "auto") -> int:
+    a = make_args(di, algo=algo)
+    n = load().mla_verify_workspace_size(ctypes.byref(a), int(num_splits))
+    if n == 0 and di.B > 0 and di.Q > 0:
+        raise MlaError(MLA_ERR_INVALID_ARG, "mla_verify_workspace_size")
+    return int(n)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(stream.cuda_stream))
+
+
+def alloc_workspace(nbytes: int, device="cuda"):
+    import torch
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def verify_attn(di: DeviceInputs, out=None, lse=None, num_splits: int = 0, algo: str = "auto",
+                workspace=None, stream=None, profile_events=None):
+    """Run mla_verify_attn; returns (out [B,Q,H,512], lse [B,Q,H] fp32)."""
+    import torch
+    dev = di.q_lat.device
+    odt = torch.bfloat16 if di.dtype == "bf16" else torch.float32
+    if out is None:
+        out = torch.empty((di.B, di.Q, di.H, 512), dtype=odt, device=dev)
+    if lse is None:
+        lse = torch.empty((di.B, di.Q, di.H), dtype=torch.float32, device=dev)
+    a = make_args(di, out, lse, algo, profile_events)
+    lib = load()
+    need = lib.mla_verify_workspace_size(ctypes.byref(a), int(num_splits))
+    if workspace is None:
+        workspace = alloc_workspace(need, dev)
+    st = lib.mla_verify_attn(ctypes.byref(a), ctypes.c_void_p(_ptr(workspace)),
+                             ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                             int(num_splits), _stream(stream))
+    if st != MLA_OK:
+        raise MlaError(st, "mla_verify_attn")
+    return out, lse
+
+
+def build_meta(di: DeviceInputs, workspace=None, stream=None):
+    """Run mla_verify_build_meta; returns (anc [B,Q] uint64 as int64, slots [sum N_b] int32)."""
+    import torch
+    dev = di.q_lat.device
+    a = make_args(di)
+    lib = load()
+    need = lib.mla_verify_workspace_size(ctypes.byref(a), 1)
+    if workspace is None:
+        workspace = alloc_workspace(need, dev)
+    total = int((di.prefix_lens.to(torch.int64) + di.Q).sum().item())
+    anc = torch.zeros((di.B, di.Q), dtype=torch.int64, device=dev)
+    slots = torch.full((max(total, 1),), -7, dtype=torch.int32, device=dev)
+    st = lib.mla_verify_build_meta(ctypes.byref(a), ctypes.c_void_p(_ptr(workspace)),
+                                   ctypes.c_size_t(workspace.numel()), ctypes.c_void_p(_ptr(anc)),
+                                   ctypes.c_void_p(_ptr(slots)), ctypes.c_int64(total), _stream(stream))
+    if st != MLA_OK:
+        raise MlaError(st, "mla_verify_build_meta")
+    return anc, slots[:total], workspace
+
+
+def check(workspace, stream=None) -> int:
+    """Synchronise and return the device error bits of the last call on this workspace."""
+    bits = ctypes.c_uint32(0)
+    st = load().mla_verify_check(ctypes.c_void_p(_ptr(workspace)), _stream(stream), ctypes.byref(bits))
+    if st not in (MLA_OK, MLA_ERR_DEVICE_CHECK):
+        raise MlaError(st, "mla_verify_check")
+    return int(bits.value)

@@ -1,0 +1,241 @@
+// C ABI of the verify-attention library: argument validation, the work
+// partition, workspace carving and the launch sequence
+//   metadata kernel -> split-KV attention kernel -> LSE combine
+// on the caller's stream.  Nothing here allocates device memory or
+// synchronises the host (mla_verify_check excepted, by design).
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace mlav {
+cudaError_t launch_meta(const Params& p, int sm_count, int32_t* slots_out, int64_t capacity,
+                        uint64_t* anc_out, cudaStream_t stream);
+cudaError_t launch_attn_simt(const Params& p, cudaStream_t stream);
+cudaError_t launch_combine(const Params& p, cudaStream_t stream);
+int simt_rows_per_group();
+int simt_tokens_per_tile();
+cudaError_t launch_attn_tc(const Params& p, cudaStream_t stream);
+int tc_rows_per_group();
+int tc_tokens_per_tile();
+int tc_units_auto(int sm_count);
+int tc_default_for(int dtype);
+}  // namespace mlav
+
+using namespace mlav;
+
+namespace {
+
+struct Plan {
+  int algo;        // MLA_ALGO_SIMT or MLA_ALGO_TC (resolved)
+  int rg, tk, groups;
+  int64_t units;
+  int sm_count;
+  WsLayout L;
+  bool noop;
+};
+
+int device_sm_count(int* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  *out = n;
+  return 0;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+mla_status validate(const mla_verify_args* a) {
+  if (!a) return MLA_ERR_INVALID_ARG;
+  if (a->B < 0 || a->Q < 0 || a->H < 1) return MLA_ERR_INVALID_ARG;
+  if (a->Q > MLA_MAX_Q) return MLA_ERR_UNSUPPORTED;
+  if (a->dtype != MLA_BF16 && a->dtype != MLA_FP32) return MLA_ERR_INVALID_ARG;
+  if (a->algo != MLA_ALGO_AUTO && a->algo != MLA_ALGO_SIMT && a->algo != MLA_ALGO_TC)
+    return MLA_ERR_INVALID_ARG;
+  if (a->algo == MLA_ALGO_TC && a->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  if (a->B == 0 || a->Q == 0) return MLA_OK;  // nothing to compute
+  if ((int64_t)a->H * a->Q > (int64_t)1 << 24) return MLA_ERR_UNSUPPORTED;
+  if (!a->q_lat || !a->q_pe || !a->kv_c || !a->k_pe || !a->prefix_lens || !a->tree_parent || !a->out)
+    return MLA_ERR_INVALID_ARG;
+  if (a->kv_c_stride < MLA_DL || a->k_pe_stride < MLA_DR || a->pool_slots < 1 ||
+      a->pool_slots > INT32_MAX)
+    return MLA_ERR_INVALID_ARG;
+  const int el = a->dtype == MLA_BF16 ? 2 : 4;
+  if ((a->kv_c_stride * el) % 16 || (a->k_pe_stride * el) % 16) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(a->q_lat) || !aligned16(a->q_pe) || !aligned16(a->kv_c) || !aligned16(a->k_pe) ||
+      !aligned16(a->out))
+    return MLA_ERR_INVALID_ARG;
+  if (a->page_size < 1) return MLA_ERR_INVALID_ARG;
+  if (a->page_size == 1) {
+    if (!a->kv_indptr || !a->kv_indices) return MLA_ERR_INVALID_ARG;
+  } else {
+    if (!a->block_table || a->max_pages < 1) return MLA_ERR_INVALID_ARG;
+    if ((int64_t)a->max_pages * a->page_size > INT32_MAX) return MLA_ERR_INVALID_ARG;
+  }
+  if (!std::isfinite(a->scale)) return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+// num_splits: 0 = auto (needs a device), > 0 = about that many pieces per row group.
+mla_status make_plan(const mla_verify_args* a, int num_splits, Plan* pl) {
+  mla_status st = validate(a);
+  if (st != MLA_OK) return st;
+  if (num_splits < 0) return MLA_ERR_INVALID_ARG;
+  std::memset(pl, 0, sizeof(*pl));
+  pl->noop = (a->B == 0 || a->Q == 0);
+  int algo = a->algo;
+  if (algo == MLA_ALGO_AUTO) algo = tc_default_for(a->dtype);
+  pl->algo = algo;
+  if (algo == MLA_ALGO_TC) {
+    pl->rg = tc_rows_per_group();
+    pl->tk = tc_tokens_per_tile();
+  } else {
+    pl->rg = simt_rows_per_group();
+    pl->tk = simt_tokens_per_tile();
+  }
+  const int64_t rows = (int64_t)a->H * a->Q;
+  pl->groups = (int)((rows + pl->rg - 1) / pl->rg);
+  if (pl->noop) {
+    pl->units = 0;
+    pl->L = ws_layout(0, 0, pl->rg, 0);
+    return MLA_OK;
+  }
+  if (num_splits == 0) {
+    if (device_sm_count(&pl->sm_count) != 0) return MLA_ERR_CUDA;
+  }
+  if (num_splits > 0) {
+    pl->units = (int64_t)num_splits * a->B * pl->groups;
+  } else if (algo == MLA_ALGO_TC) {
+    pl->units = tc_units_auto(pl->sm_count);
+  } else {
+    pl->units = (int64_t)pl->sm_count * 2;
+  }
+  if (pl->units < 1) pl->units = 1;
+  if (pl->units > ((int64_t)1 << 22)) return MLA_ERR_UNSUPPORTED;
+  pl->L = ws_layout(a->B, a->Q, pl->rg, pl->units + (int64_t)a->B * pl->groups);
+  return MLA_OK;
+}
+
+Params make_params(const mla_verify_args* a, const Plan& pl, void* ws) {
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.B = a->B;
+  p.Q = a->Q;
+  p.H = a->H;
+  p.rows = a->H * a->Q;
+  p.dtype = a->dtype;
+  p.q_lat = a->q_lat;
+  p.q_pe = a->q_pe;
+  p.kv_c = a->kv_c;
+  p.k_pe = a->k_pe;
+  p.kv_c_stride = a->kv_c_stride;
+  p.k_pe_stride = a->k_pe_stride;
+  p.pool_slots = a->pool_slots;
+  p.page_size = a->page_size;
+  p.kv_indptr = a->kv_indptr;
+  p.kv_indices = a->kv_indices;
+  p.block_table = a->block_table;
+  p.max_pages = a->max_pages;
+  p.prefix_lens = a->prefix_lens;
+  p.tree_parent = a->tree_parent;
+  p.scale = a->scale;
+  p.scale_log2 = (float)((double)a->scale * 1.4426950408889634);
+  p.out = a->out;
+  p.lse = a->lse;
+  p.rg = pl.rg;
+  p.groups = pl.groups;
+  p.tk = pl.tk;
+  p.units = (int)pl.units;
+  char* base = static_cast<char*>(ws);
+  p.err = reinterpret_cast<uint32_t*>(base + pl.L.err);
+  p.anc = reinterpret_cast<uint64_t*>(base + pl.L.anc);
+  p.seq_tiles = reinterpret_cast<int32_t*>(base + pl.L.seq_tiles);
+  p.seq_base = reinterpret_cast<int64_t*>(base + pl.L.seq_base);
+  p.seq_kv_base = reinterpret_cast<int64_t*>(base + pl.L.seq_kv_base);
+  p.part_lse = reinterpret_cast<float*>(base + pl.L.part_lse);
+  p.part_o = reinterpret_cast<float*>(base + pl.L.part_o);
+  return p;
+}
+
+mla_status check_ws(const Plan& pl, const void* ws, size_t ws_bytes) {
+  if (!ws) return MLA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return MLA_ERR_WORKSPACE;
+  if (ws_bytes < pl.L.total) return MLA_ERR_WORKSPACE;
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mla_verify_workspace_size(const mla_verify_args* a, int num_splits) {
+  Plan pl;
+  if (make_plan(a, num_splits, &pl) != MLA_OK) return 0;
+  return pl.L.total;
+}
+
+mla_status mla_verify_attn(const mla_verify_args* a, void* workspace, size_t ws_bytes, int num_splits,
+                           mla_stream_t stream) {
+  Plan pl;
+  mla_status st = make_plan(a, num_splits, &pl);
+  if (st != MLA_OK) return st;
+  if (pl.noop) return MLA_OK;
+  st = check_ws(pl, workspace, ws_bytes);
+  if (st != MLA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (pl.sm_count == 0 && device_sm_count(&pl.sm_count) != 0) return MLA_ERR_CUDA;
+  const Params p = make_params(a, pl, workspace);
+  if (launch_meta(p, pl.sm_count, nullptr, 0, nullptr, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (a->profile_events && cudaEventRecord((cudaEvent_t)a->profile_events[0], s) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  cudaError_t e = (pl.algo == MLA_ALGO_TC) ? launch_attn_tc(p, s) : launch_attn_simt(p, s);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  if (a->profile_events && cudaEventRecord((cudaEvent_t)a->profile_events[1], s) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (launch_combine(p, s) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+mla_status mla_verify_build_meta(const mla_verify_args* a, void* workspace, size_t ws_bytes, uint64_t* anc,
+                                 int32_t* slots, int64_t slots_capacity, mla_stream_t stream) {
+  Plan pl;
+  mla_status st = make_plan(a, 1, &pl);
+  if (st != MLA_OK) return st;
+  if (pl.noop) return MLA_OK;
+  if (!anc || !slots || slots_capacity < 0) return MLA_ERR_INVALID_ARG;
+  st = check_ws(pl, workspace, ws_bytes);
+  if (st != MLA_OK) return st;
+  if (device_sm_count(&pl.sm_count) != 0) return MLA_ERR_CUDA;
+  const Params p = make_params(a, pl, workspace);
+  if (launch_meta(p, pl.sm_count, slots, slots_capacity, anc, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+mla_status mla_verify_check(const void* workspace, mla_stream_t stream, uint32_t* bits) {
+  if (!workspace) return MLA_ERR_WORKSPACE;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+  uint32_t v = 0;
+  // the error word sits at offset 0 of every workspace layout
+  if (cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+  if (bits) *bits = v;
+  return v ? MLA_ERR_DEVICE_CHECK : MLA_OK;
+}
+
+const char* mla_status_str(mla_status s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+    case MLA_ERR_DEVICE_CHECK: return "MLA_ERR_DEVICE_CHECK";
+  }
+  return "MLA_ERR_UNKNOWN";
+}
+
+int mla_verify_abi_version(void) { return MLA_VERIFY_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,146 @@
+// Metadata kernels: ancestor-or-self masks of every draft tree, per-sequence
+// tile counts and their prefix sums (the linear work space the attention
+// kernels partition), and validation of every device-resident table entry.
+//
+// The mask rule follows "Reading the Reference: How a Single File-Read Message
+// Anchored a Complex CUDA Kernel Implementation", section "Output Knowledge
+// Created by This Message" (prefix visibility + tree-tail visibility) and
+// "Ground Truth in Silicon ...", section "Input Knowledge Required ...",
+// item 3: node i sees tree node t when t is i or an ancestor of i.  With nodes
+// in topological order (parent[i] < i) the set is built in one forward pass:
+// anc[i] = bit(i) | anc[parent[i]].
+#include "common.cuh"
+
+namespace mlav {
+
+constexpr int kMetaThreads = 1024;
+
+// Block-wide inclusive scan of one value per thread (kMetaThreads threads).
+__device__ int64_t block_inclusive_scan(int64_t v, int64_t* sh) {
+  const int tid = threadIdx.x;
+  sh[tid] = v;
+  __syncthreads();
+  for (int off = 1; off < kMetaThreads; off <<= 1) {
+    int64_t add = (tid >= off) ? sh[tid - off] : 0;
+    __syncthreads();
+    sh[tid] += add;
+    __syncthreads();
+  }
+  int64_t r = sh[tid];
+  __syncthreads();
+  return r;
+}
+
+// One block.  Clears the error word, validates prefix_lens / kv_indptr /
+// page capacity / parents, builds anc, T_b = ceil(N_b / tk), and the prefix
+// sums seq_base (G * T_b) and seq_kv_base (N_b).
+__global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
+  __shared__ int64_t sh[kMetaThreads];
+  __shared__ int64_t carry_work, carry_kv;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    *p.err = 0u;
+    carry_work = 0;
+    carry_kv = 0;
+    p.seq_base[0] = 0;
+    p.seq_kv_base[0] = 0;
+  }
+  __syncthreads();
+
+  for (int b0 = 0; b0 < p.B; b0 += kMetaThreads) {
+    const int b = b0 + tid;
+    int64_t work = 0, nkv = 0;
+    if (b < p.B) {
+      int64_t P = p.prefix_lens[b];
+      uint32_t e = 0;
+      if (P < 0) { e |= MLA_DEVERR_PREFIX; P = 0; }
+      const int64_t N = P + p.Q;
+      if (p.page_size == 1) {
+        const int64_t lo = p.kv_indptr[b], hi = p.kv_indptr[b + 1];
+        // with kv_indptr[0] == 0 and every span equal to N_b, all reads stay in
+        // kv_indices[0 .. kv_indptr[B])
+        if ((b == 0 && lo != 0) || lo < 0 || hi - lo != N) e |= MLA_DEVERR_INDPTR;
+      } else if (N > (int64_t)p.max_pages * p.page_size) {
+        e |= MLA_DEVERR_PAGES;
+      }
+      // ancestor-or-self masks
+      uint64_t anc_local[MLA_MAX_Q];
+      for (int i = 0; i < p.Q; ++i) {
+        int par = p.tree_parent[(int64_t)b * p.Q + i];
+        if (par < -1 || par >= i) { e |= MLA_DEVERR_PARENT; par = -1; }
+        const uint64_t self = 1ull << i;
+        anc_local[i] = (par < 0) ? self : (anc_local[par] | self);
+        p.anc[(int64_t)b * p.Q + i] = anc_local[i];
+      }
+      if (e) set_err(p.err, e);
+      const int64_t T = (N + p.tk - 1) / p.tk;
+      p.seq_tiles[b] = (int32_t)T;
+      work = T * p.groups;
+      nkv = N;
+    }
+    const int64_t w_inc = block_inclusive_scan(work, sh);
+    const int64_t k_inc = block_inclusive_scan(nkv, sh);
+    if (b < p.B) {
+      p.seq_base[b + 1] = carry_work + w_inc;
+      p.seq_kv_base[b + 1] = carry_kv + k_inc;
+    }
+    __syncthreads();
+    if (tid == kMetaThreads - 1) {
+      carry_work += w_inc;
+      carry_kv += k_inc;
+    }
+    __syncthreads();
+  }
+}
+
+// Grid-stride pass over every (sequence, position): checks that each resolved
+// slot lies in the pool and, when slots_out is given, records it.  Skips all
+// table reads if the sequence-level checks already failed (an inconsistent
+// indptr would make the index arithmetic itself unsafe).
+__global__ void meta_slots_kernel(Params p, int32_t* slots_out, int64_t capacity) {
+  if (*p.err & (MLA_DEVERR_PREFIX | MLA_DEVERR_INDPTR | MLA_DEVERR_PAGES)) return;
+  const int64_t total = p.seq_kv_base[p.B];
+  uint32_t e = 0;
+  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < total;
+       k += (int64_t)gridDim.x * blockDim.x) {
+    const int b = seq_of(p.seq_kv_base, p.B, k);
+    const int64_t pos = k - p.seq_kv_base[b];
+    int64_t s;
+    if (p.page_size == 1) {
+      s = p.kv_indices[(int64_t)p.kv_indptr[b] + pos];
+    } else {
+      s = (int64_t)p.block_table[(int64_t)b * p.max_pages + pos / p.page_size] * p.page_size +
+          pos % p.page_size;
+    }
+    if (s < 0 || s >= p.pool_slots) e |= MLA_DEVERR_SLOT;
+    if (slots_out) {
+      if (k < capacity) slots_out[k] = (int32_t)s;
+      else e |= MLA_DEVERR_CAPACITY;
+    }
+  }
+  if (e) set_err(p.err, e);
+}
+
+__global__ void copy_anc_kernel(Params p, uint64_t* anc_out) {
+  const int64_t n = (int64_t)p.B * p.Q;
+  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < n;
+       k += (int64_t)gridDim.x * blockDim.x)
+    anc_out[k] = p.anc[k];
+}
+
+cudaError_t launch_meta(const Params& p, int sm_count, int32_t* slots_out, int64_t capacity,
+                        uint64_t* anc_out, cudaStream_t stream) {
+  meta_seq_kernel<<<1, kMetaThreads, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  meta_slots_kernel<<<2 * sm_count, 256, 0, stream>>>(p, slots_out, capacity);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (anc_out) {
+    copy_anc_kernel<<<64, 256, 0, stream>>>(p, anc_out);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace mlav

@@ -1,0 +1,128 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol,
+and rejects malformed arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mla_tree_verify_absorbed_gb300 import api, build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla_verify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return api.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == set(api.EXPORTS), names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.mla_verify_abi_version() == 1
+    assert api.status_str(0) == "MLA_OK"
+    assert api.status_str(5) == "MLA_ERR_DEVICE_CHECK"
+
+
+def test_struct_layout_matches_header(lib):
+    # offsets of a few fields under the C ABI on LP64 (natural alignment)
+    A = api.MlaVerifyArgs
+    assert A.q_lat.offset == 16 and A.kv_c_stride.offset == 48 and A.page_size.offset == 72
+    assert A.kv_indptr.offset == 80 and A.max_pages.offset == 104
+    assert A.scale.offset == 128 and A.out.offset == 136 and A.algo.offset == 152
+    assert A.profile_events.offset == 160 and ctypes.sizeof(A) == 168
+
+
+def fake_args(**kw):
+    """Well-formed arguments with fake (never dereferenced on the host) pointers."""
+    a = api.MlaVerifyArgs()
+    a.B, a.Q, a.H, a.dtype = 2, 8, 16, api.MLA_BF16
+    p = 0x10000
+    for f in ("q_lat", "q_pe", "kv_c", "k_pe", "kv_indptr", "kv_indices", "prefix_lens",
+              "tree_parent", "out", "lse"):
+        setattr(a, f, p)
+        p += 0x10000
+    a.kv_c_stride, a.k_pe_stride, a.pool_slots = 576, 576, 1000
+    a.page_size, a.scale, a.algo = 1, 0.07, api.ALGO["simt"]
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def attn(lib, a, ws=0x100000, nbytes=1 << 40, splits=1):
+    return lib.mla_verify_attn(ctypes.byref(a), ctypes.c_void_p(ws), ctypes.c_size_t(nbytes), splits, None)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("B", -1, api.MLA_ERR_INVALID_ARG),
+    ("H", 0, api.MLA_ERR_INVALID_ARG),
+    ("Q", 65, api.MLA_ERR_UNSUPPORTED),
+    ("dtype", 7, api.MLA_ERR_INVALID_ARG),
+    ("algo", 9, api.MLA_ERR_INVALID_ARG),
+    ("q_lat", None, api.MLA_ERR_INVALID_ARG),
+    ("out", None, api.MLA_ERR_INVALID_ARG),
+    ("kv_indices", None, api.MLA_ERR_INVALID_ARG),
+    ("kv_c_stride", 511, api.MLA_ERR_INVALID_ARG),
+    ("kv_c_stride", 516, api.MLA_ERR_INVALID_ARG),      # 1032 bytes: not a multiple of 16
+    ("k_pe_stride", 60, api.MLA_ERR_INVALID_ARG),
+    ("pool_slots", 0, api.MLA_ERR_INVALID_ARG),
+    ("page_size", 0, api.MLA_ERR_INVALID_ARG),
+    ("kv_c", 0x10008, api.MLA_ERR_INVALID_ARG),         # not 16-byte aligned
+    ("scale", float("nan"), api.MLA_ERR_INVALID_ARG),
+])
+def test_host_validation(lib, field, value, status):
+    a = fake_args(**{field: value})
+    assert attn(lib, a) == status
+    assert lib.mla_verify_workspace_size(ctypes.byref(a), 1) == 0
+
+
+def test_tc_requires_bf16(lib):
+    a = fake_args(dtype=api.MLA_FP32, algo=api.ALGO["tc"])
+    assert attn(lib, a) == api.MLA_ERR_UNSUPPORTED
+
+
+def test_paged_needs_block_table(lib):
+    a = fake_args(page_size=64, kv_indptr=None, kv_indices=None)
+    assert attn(lib, a) == api.MLA_ERR_INVALID_ARG
+    a = fake_args(page_size=64, block_table=0x900000, max_pages=0)
+    assert attn(lib, a) == api.MLA_ERR_INVALID_ARG
+
+
+def test_noop_shapes(lib):
+    for kw in (dict(B=0), dict(Q=0)):
+        a = fake_args(**kw)
+        assert attn(lib, a, ws=0, nbytes=0) == api.MLA_OK
+
+
+def test_workspace_checks(lib):
+    a = fake_args()
+    need = lib.mla_verify_workspace_size(ctypes.byref(a), 1)
+    assert need > 0
+    assert attn(lib, a, ws=0) == api.MLA_ERR_WORKSPACE
+    assert attn(lib, a, ws=0x100010) == api.MLA_ERR_WORKSPACE          # not 256-byte aligned
+    assert attn(lib, a, nbytes=need - 1) == api.MLA_ERR_WORKSPACE
+    # more splits never need less workspace; both kernel families size it
+    assert lib.mla_verify_workspace_size(ctypes.byref(a), 4) >= need
+    b = fake_args(algo=api.ALGO["tc"])
+    assert lib.mla_verify_workspace_size(ctypes.byref(b), 3) > 0
+    assert lib.mla_verify_workspace_size(ctypes.byref(a), -1) == 0
+
+
+def test_build_meta_validation(lib):
+    a = fake_args()
+    st = lib.mla_verify_build_meta(ctypes.byref(a), ctypes.c_void_p(0x100000), ctypes.c_size_t(1 << 40),
+                                   None, ctypes.c_void_p(0x200000), ctypes.c_int64(10), None)
+    assert st == api.MLA_ERR_INVALID_ARG

@@ -1,0 +1,217 @@
+"""CUDA path against the CPU oracle, through the C ABI (needs a GPU)."""
+import numpy as np
+import pytest
+
+import oracle
+from mla_tree_verify_absorbed_gb300 import api
+from mla_tree_verify_absorbed_gb300 import inputs as I
+from tests import parity as PT
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+ALGOS_BF16 = ["simt", "tc"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    api.load()
+
+
+def run(p, algo="auto", num_splits=0, separate_pools=False, **kw):
+    di = api.device_inputs(p, separate_pools=separate_pools)
+    out, lse = api.verify_attn(di, num_splits=num_splits, algo=algo, **kw)
+    torch.cuda.synchronize()
+    return di, out, lse
+
+
+# ---------------------------------------------------------------------------
+# a1 / a2: tree masks and slot resolution, bit-exact
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name", I.CONFIG_NAMES)
+def test_meta_bitexact(name):
+    p = PT.workload(name)
+    di = api.device_inputs(p)
+    anc, slots, ws = api.build_meta(di)
+    assert api.check(ws) == 0
+    want_anc = oracle.get().tree_anc(p.tree_parent)
+    got_anc = anc.cpu().numpy().view(np.uint64)
+    assert np.array_equal(got_anc, want_anc)
+    want_slots = oracle.get().resolve_slots(p)
+    assert np.array_equal(slots.cpu().numpy(), want_slots)
+
+
+# ---------------------------------------------------------------------------
+# small problems: every output element against the oracle
+# ---------------------------------------------------------------------------
+def mid_problem(seed=21, layout="scattered"):
+    kw = dict(name="mid", dtype="bf16", B=2, H=64, Q=16, prefix_lens=[300, 777], seed=seed)
+    if layout == "paged":
+        kw.update(layout="paged", page_size=64, n_pages=40)
+    else:
+        kw.update(layout="scattered", pool_slots=2048)
+    return I.make_problem(**kw)
+
+
+def ragged_problem():
+    # rows = 5 heads x 7 nodes = 35 (not a multiple of any row group), tiny and
+    # empty prefixes, paged with page_size 16
+    return I.make_problem(name="ragged", dtype="bf16", B=3, H=5, Q=7, prefix_lens=[0, 1, 130],
+                          seed=22, layout="paged", page_size=16, n_pages=20)
+
+
+def check_all_rows(p, out, lse, what):
+    rows = I.all_rows(p)
+    ro, rl = PT.oracle_rows(p, rows)
+    go, gl = PT.gather_rows(out, lse, rows)
+    PT.assert_close(go, ro, p.dtype, what + " out")
+    PT.assert_close(gl, rl, p.dtype, what + " lse")
+
+
+def test_tiny_fp32():
+    p = PT.workload("tiny")
+    _, out, lse = run(p)
+    check_all_rows(p, out, lse, "tiny")
+
+
+@pytest.mark.parametrize("algo", ALGOS_BF16)
+@pytest.mark.parametrize("maker", [mid_problem, ragged_problem,
+                                   lambda: mid_problem(23, "paged")],
+                         ids=["mid_scattered", "ragged_paged", "mid_paged"])
+def test_full_rows_bf16(algo, maker):
+    p = maker()
+    _, out, lse = run(p, algo=algo)
+    check_all_rows(p, out, lse, f"{p.name}/{algo}")
+
+
+def test_tiny_fp32_via_simt_bf16_shape():
+    # the same tiny tree through the bf16 cache and both kernel families
+    p = I.make_problem(name="tiny_bf16", dtype="bf16", B=1, H=16, Q=8, prefix_lens=[256], seed=0,
+                       trees=[I.TINY_TREE])
+    for algo in ALGOS_BF16:
+        _, out, lse = run(p, algo=algo)
+        check_all_rows(p, out, lse, f"tiny_bf16/{algo}")
+
+
+@pytest.mark.parametrize("algo", ALGOS_BF16)
+def test_split_invariance(algo):
+    p = mid_problem(24)
+    rows = I.all_rows(p)
+    ro, rl = PT.oracle_rows(p, rows)
+    results = []
+    for ns in (1, 2, 7, 0):
+        _, out, lse = run(p, algo=algo, num_splits=ns)
+        go, gl = PT.gather_rows(out, lse, rows)
+        PT.assert_close(go, ro, "bf16", f"splits={ns} out")
+        PT.assert_close(gl, rl, "bf16", f"splits={ns} lse")
+        results.append((go, gl))
+    for go, gl in results[1:]:
+        # pieces only change fp32 summation order: a couple of bf16 ulps at most
+        assert np.abs(go - results[0][0]).max() <= 2e-2 * np.abs(results[0][0]).max()
+        assert np.abs(gl - results[0][1]).max() <= 1e-4 * np.abs(results[0][1]).max() + 1e-5
+
+
+@pytest.mark.parametrize("algo", ALGOS_BF16)
+def test_needles(algo):
+    p = mid_problem(25)
+    I.plant_needles(p, seed=5)
+    _, out, lse = run(p, algo=algo)
+    rows = I.all_rows(p)
+    ro, rl = PT.oracle_rows(p, rows)
+    go, gl = PT.gather_rows(out, lse, rows)
+    # the softmax is peaked: outputs are O(1), a wrong gather or mask moves them by O(1)
+    assert np.abs(ro).max() > 1.0
+    PT.assert_close(go, ro, "bf16", "needle out")
+    PT.assert_close(gl, rl, "bf16", "needle lse")
+
+
+@pytest.mark.parametrize("algo", ALGOS_BF16)
+def test_separate_pools(algo):
+    p = mid_problem(26)
+    _, out, lse = run(p, algo=algo, separate_pools=True)
+    check_all_rows(p, out, lse, "separate pools")
+
+
+@pytest.mark.parametrize("algo", ALGOS_BF16)
+def test_edge_trees(algo):
+    # every node a root over an empty prefix: each row sees only itself
+    p = I.make_problem(name="roots", dtype="bf16", B=2, H=4, Q=5, prefix_lens=[0, 0], seed=27,
+                       trees=[[-1] * 5, [-1, 0, -1, 2, 3]])
+    _, out, lse = run(p, algo=algo)
+    check_all_rows(p, out, lse, "roots")
+    # a 64-node chain: the last node's mask uses bit 63
+    p = I.make_problem(name="chain64", dtype="bf16", B=1, H=2, Q=64, prefix_lens=[10], seed=28,
+                       trees=[list(range(-1, 63))])
+    _, out, lse = run(p, algo=algo)
+    check_all_rows(p, out, lse, "chain64")
+    # a single node, a single head
+    p = I.make_problem(name="q1", dtype="bf16", B=3, H=1, Q=1, prefix_lens=[5, 0, 64], seed=29)
+    _, out, lse = run(p, algo=algo)
+    check_all_rows(p, out, lse, "q1")
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, in the launch configuration the benchmark times
+# (num_splits = 0, default kernel family): sampled rows against the oracle
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name,heads,needles", [
+    ("c2", 8, False), ("c2", 4, True), ("c3", 2, False), ("c3", 2, True),
+    ("c4", 2, False), ("c5", 2, False),
+])
+def test_full_size_sampled(name, heads, needles):
+    p = PT.workload(name, needles)
+    _, out, lse = run(p)
+    rows = I.sample_rows(p, heads, seed=31)
+    ro, rl = PT.oracle_rows(p, rows)
+    go, gl = PT.gather_rows(out, lse, rows)
+    PT.assert_close(go, ro, p.dtype, f"{name} out")
+    PT.assert_close(gl, rl, p.dtype, f"{name} lse")
+    # properties that hold at any size: finite everywhere, lse >= max visible score bound
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
+# ---------------------------------------------------------------------------
+# device-side table checks (bad contents never reach an address; the
+# error word reports them and outputs are left untouched)
+# ---------------------------------------------------------------------------
+def _poisoned(p, field):
+    di = api.device_inputs(p)
+    if field == "slot":
+        di.kv_indices[5] = di.pool_slots          # one past the pool
+        want = 0x4
+    elif field == "parent":
+        di.tree_parent[0, 3] = 3                  # a node may not be its own parent
+        want = 0x8
+    elif field == "indptr":
+        di.kv_indptr[1] += 1                      # span disagrees with prefix_lens + Q
+        want = 0x2
+    elif field == "prefix":
+        di.prefix_lens[0] = -4
+        want = 0x1
+    return di, want
+
+
+@pytest.mark.parametrize("field", ["slot", "parent", "indptr", "prefix"])
+def test_device_table_errors(field):
+    p = mid_problem(30)
+    di, want = _poisoned(p, field)
+    out = torch.full((p.B, p.Q, p.H, 512), 7.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((p.B, p.Q, p.H), 7.0, dtype=torch.float32, device="cuda")
+    ws = api.alloc_workspace(api.workspace_size(di, 0))
+    api.verify_attn(di, out=out, lse=lse, workspace=ws)
+    bits = api.check(ws)
+    assert bits & want, hex(bits)
+    assert (out.float() == 7.0).all() and (lse == 7.0).all()
+    # the same workspace is clean again after a good call
+    di2 = api.device_inputs(p)
+    api.verify_attn(di2, workspace=ws)
+    assert api.check(ws) == 0
+
+
+def test_noop_shapes():
+    p = I.make_problem(name="empty", dtype="bf16", B=1, H=4, Q=0, prefix_lens=[12], seed=1)
+    di = api.device_inputs(p)
+    out, lse = api.verify_attn(di)
+    assert out.numel() == 0
