@@ -123,11 +123,12 @@ size_t mla_verify_workspace_size(const mla_verify_args *args, int num_splits);
  * group's KV was cut into several pieces, the LSE-combine kernel, all on
  * `stream`.  workspace: device memory of at least
  * mla_verify_workspace_size(args, num_splits) bytes, 256-byte aligned, not
- * used concurrently by another call.  num_splits: 0 picks a partition that
- * fills the GPU once; n > 0 cuts the KV work of each 128-row group (16-row
- * group for the SIMT kernel) into about n pieces (exactly n when all
- * sequences have the same length).  Results do not depend on num_splits
- * beyond fp32 rounding. */
+ * used concurrently by another call.  num_splits: n > 0 cuts the KV range
+ * of every row group (128 query rows for the tensor-core kernel, 16 for the
+ * SIMT kernel) into exactly n chunks, merged by the LSE-combine kernel when
+ * n > 1 (a chunk is empty when a sequence has fewer than n KV tiles); 0 picks
+ * n from B, H, Q and the SM count so the work items fill the GPU in whole
+ * waves.  Results do not depend on num_splits beyond fp32 rounding. */
 mla_status mla_verify_attn(const mla_verify_args *args, void *workspace, size_t ws_bytes,
                            int num_splits, mla_stream_t stream);
 

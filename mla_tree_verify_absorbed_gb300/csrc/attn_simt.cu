@@ -2,8 +2,8 @@
 //
 // It is the kernel for the fp32 cache (a 1e-4 relative tolerance needs fp32
 // products, which the bf16 tensor-core path cannot give) and an explicit
-// alternative for bf16.  Structure: a CTA takes one work unit of the linear
-// (sequence, row group, KV tile) space; for each row group piece it keeps the
+// alternative for bf16.  Structure: CTAs take work items (sequence, KV chunk,
+// row group) round-robin; for each item a CTA keeps the
 // group's 16 absorbed query rows in shared memory, stages 32-token KV tiles
 // (kv_c and k_pe of each token, gathered through the slot table) once, and
 // reuses each staged tile for every row of the group -- the head-tile reuse
@@ -44,15 +44,9 @@ __global__ void __launch_bounds__(kSimtThreads, 2) attn_simt_kernel(Params p) {
   const T* k_pe = reinterpret_cast<const T*>(p.k_pe);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t W = p.seq_base[p.B];
-  const int64_t U = p.units;
-  const int64_t c = blockIdx.x;
-  if (c >= U || W == 0) return;
-  const int64_t lo = unit_lo(c, W, U), hi = unit_lo(c + 1, W, U);
-
-  for (int64_t x = lo; x < hi;) {
-    const Segment sg = segment_at(p, x, hi);
-    x += sg.t1 - sg.t0;
+  for (int64_t item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+    const Item sg = item_at(p, item);
+    if (sg.t1 <= sg.t0) continue;  // empty chunk (sequence shorter than the split count)
     const int b = sg.b;
     const int64_t P = p.prefix_lens[b];
     const int64_t N = P + p.Q;
@@ -170,14 +164,13 @@ __global__ void __launch_bounds__(kSimtThreads, 2) attn_simt_kernel(Params p) {
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
       const float lse = (l > 0.f) ? (m + log2f(l)) * ln2 : -INFINITY;
       const float* o = rr ? oB : oA;
-      if (sg.whole) {
+      if (p.splits == 1) {
         const int64_t orow = (int64_t)b * p.rows + row;
 #pragma unroll
         for (int k = 0; k < 16; ++k) store_out(p.out, p.dtype, orow * kDl + lane + 32 * k, o[k] * inv);
         if (lane == 0 && p.lse) p.lse[orow] = lse;
       } else {
-        const int64_t slot = part_slot(c, b, sg.g, p.groups);
-        const int64_t prow = slot * kSimtRG + (row - row0);
+        const int64_t prow = item * kSimtRG + (row - row0);
 #pragma unroll
         for (int k = 0; k < 16; ++k) p.part_o[prow * kDl + lane + 32 * k] = o[k] * inv;
         if (lane == 0) p.part_lse[prow] = lse;
@@ -187,7 +180,7 @@ __global__ void __launch_bounds__(kSimtThreads, 2) attn_simt_kernel(Params p) {
 }
 
 cudaError_t launch_attn_simt(const Params& p, cudaStream_t stream) {
-  const int grid = p.units;
+  const int grid = p.grid;
   if (p.dtype == MLA_BF16) {
     cudaFuncSetAttribute(attn_simt_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSimtSmem);
     attn_simt_kernel<__nv_bfloat16><<<grid, kSimtThreads, kSimtSmem, stream>>>(p);
@@ -199,6 +192,7 @@ cudaError_t launch_attn_simt(const Params& p, cudaStream_t stream) {
 }
 
 int simt_rows_per_group() { return kSimtRG; }
+int simt_ctas_per_gpu(int sm_count) { return 2 * sm_count; }  // two resident CTAs per SM
 int simt_tokens_per_tile() { return kSimtTK; }
 
 }  // namespace mlav

@@ -18,7 +18,8 @@ int simt_tokens_per_tile();
 cudaError_t launch_attn_tc(const Params& p, cudaStream_t stream);
 int tc_rows_per_group();
 int tc_tokens_per_tile();
-int tc_units_auto(int sm_count);
+int tc_clusters_per_gpu(int sm_count);
+int simt_ctas_per_gpu(int sm_count);
 int tc_default_for(int dtype);
 }  // namespace mlav
 
@@ -29,7 +30,9 @@ namespace {
 struct Plan {
   int algo;        // MLA_ALGO_SIMT or MLA_ALGO_TC (resolved)
   int rg, tk, groups;
-  int64_t units;
+  int splits;      // KV chunks per row group
+  int64_t items;   // B * splits * groups
+  int grid;        // CTAs (SIMT) or clusters (TC), persistent over items
   int sm_count;
   WsLayout L;
   bool noop;
@@ -46,7 +49,8 @@ int device_sm_count(int* out) {
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
-mla_status validate(const mla_verify_args* a) {
+// Shape-level checks: everything the workspace size depends on.
+mla_status validate_shape(const mla_verify_args* a) {
   if (!a) return MLA_ERR_INVALID_ARG;
   if (a->B < 0 || a->Q < 0 || a->H < 1) return MLA_ERR_INVALID_ARG;
   if (a->Q > MLA_MAX_Q) return MLA_ERR_UNSUPPORTED;
@@ -54,17 +58,15 @@ mla_status validate(const mla_verify_args* a) {
   if (a->algo != MLA_ALGO_AUTO && a->algo != MLA_ALGO_SIMT && a->algo != MLA_ALGO_TC)
     return MLA_ERR_INVALID_ARG;
   if (a->algo == MLA_ALGO_TC && a->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
-  if (a->B == 0 || a->Q == 0) return MLA_OK;  // nothing to compute
   if ((int64_t)a->H * a->Q > (int64_t)1 << 24) return MLA_ERR_UNSUPPORTED;
-  if (!a->q_lat || !a->q_pe || !a->kv_c || !a->k_pe || !a->prefix_lens || !a->tree_parent || !a->out)
-    return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+// Table-level checks shared by every call that reads the KV tables.
+mla_status validate_tables(const mla_verify_args* a) {
+  if (!a->prefix_lens || !a->tree_parent) return MLA_ERR_INVALID_ARG;
   if (a->kv_c_stride < MLA_DL || a->k_pe_stride < MLA_DR || a->pool_slots < 1 ||
       a->pool_slots > INT32_MAX)
-    return MLA_ERR_INVALID_ARG;
-  const int el = a->dtype == MLA_BF16 ? 2 : 4;
-  if ((a->kv_c_stride * el) % 16 || (a->k_pe_stride * el) % 16) return MLA_ERR_INVALID_ARG;
-  if (!aligned16(a->q_lat) || !aligned16(a->q_pe) || !aligned16(a->kv_c) || !aligned16(a->k_pe) ||
-      !aligned16(a->out))
     return MLA_ERR_INVALID_ARG;
   if (a->page_size < 1) return MLA_ERR_INVALID_ARG;
   if (a->page_size == 1) {
@@ -73,15 +75,48 @@ mla_status validate(const mla_verify_args* a) {
     if (!a->block_table || a->max_pages < 1) return MLA_ERR_INVALID_ARG;
     if ((int64_t)a->max_pages * a->page_size > INT32_MAX) return MLA_ERR_INVALID_ARG;
   }
+  return MLA_OK;
+}
+
+// Everything the attention itself reads or writes.
+mla_status validate_call(const mla_verify_args* a) {
+  mla_status st = validate_tables(a);
+  if (st != MLA_OK) return st;
+  if (!a->q_lat || !a->q_pe || !a->kv_c || !a->k_pe || !a->prefix_lens || !a->tree_parent || !a->out)
+    return MLA_ERR_INVALID_ARG;
+  const int el = a->dtype == MLA_BF16 ? 2 : 4;
+  if ((a->kv_c_stride * el) % 16 || (a->k_pe_stride * el) % 16) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(a->q_lat) || !aligned16(a->q_pe) || !aligned16(a->kv_c) || !aligned16(a->k_pe) ||
+      !aligned16(a->out))
+    return MLA_ERR_INVALID_ARG;
   if (!std::isfinite(a->scale)) return MLA_ERR_INVALID_ARG;
   return MLA_OK;
 }
 
-// num_splits: 0 = auto (needs a device), > 0 = about that many pieces per row group.
+// Smallest split count whose items fill `slots` concurrent workers to at
+// least 90% over whole waves; failing that, the best fill for S <= 64.
+int auto_splits(int64_t row_groups, int64_t slots) {
+  int best = 1;
+  double best_eff = -1.0;
+  for (int S = 1; S <= 64; ++S) {
+    const int64_t items = row_groups * S;
+    const int64_t waves = (items + slots - 1) / slots;
+    const double eff = (double)items / (double)(waves * slots);
+    if (items >= slots && eff >= 0.9) return S;
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = S;
+    }
+  }
+  return best;
+}
+
+// num_splits: 0 = auto (needs a device), > 0 = exactly that many KV chunks per
+// row group.
 mla_status make_plan(const mla_verify_args* a, int num_splits, Plan* pl) {
-  mla_status st = validate(a);
+  mla_status st = validate_shape(a);
   if (st != MLA_OK) return st;
-  if (num_splits < 0) return MLA_ERR_INVALID_ARG;
+  if (num_splits < 0 || num_splits > 4096) return MLA_ERR_INVALID_ARG;
   std::memset(pl, 0, sizeof(*pl));
   pl->noop = (a->B == 0 || a->Q == 0);
   int algo = a->algo;
@@ -97,23 +132,22 @@ mla_status make_plan(const mla_verify_args* a, int num_splits, Plan* pl) {
   const int64_t rows = (int64_t)a->H * a->Q;
   pl->groups = (int)((rows + pl->rg - 1) / pl->rg);
   if (pl->noop) {
-    pl->units = 0;
     pl->L = ws_layout(0, 0, pl->rg, 0);
     return MLA_OK;
   }
+  const int64_t row_groups = (int64_t)a->B * pl->groups;
+  int64_t slots = 0;
   if (num_splits == 0) {
     if (device_sm_count(&pl->sm_count) != 0) return MLA_ERR_CUDA;
-  }
-  if (num_splits > 0) {
-    pl->units = (int64_t)num_splits * a->B * pl->groups;
-  } else if (algo == MLA_ALGO_TC) {
-    pl->units = tc_units_auto(pl->sm_count);
+    slots = (algo == MLA_ALGO_TC) ? tc_clusters_per_gpu(pl->sm_count) : simt_ctas_per_gpu(pl->sm_count);
+    if (slots < 1) slots = 1;
+    pl->splits = auto_splits(row_groups, slots);
   } else {
-    pl->units = (int64_t)pl->sm_count * 2;
+    pl->splits = num_splits;
   }
-  if (pl->units < 1) pl->units = 1;
-  if (pl->units > ((int64_t)1 << 22)) return MLA_ERR_UNSUPPORTED;
-  pl->L = ws_layout(a->B, a->Q, pl->rg, pl->units + (int64_t)a->B * pl->groups);
+  pl->items = row_groups * pl->splits;
+  if (pl->items > ((int64_t)1 << 26)) return MLA_ERR_UNSUPPORTED;
+  pl->L = ws_layout(a->B, a->Q, pl->rg, pl->splits > 1 ? pl->items : 0);
   return MLA_OK;
 }
 
@@ -146,12 +180,13 @@ Params make_params(const mla_verify_args* a, const Plan& pl, void* ws) {
   p.rg = pl.rg;
   p.groups = pl.groups;
   p.tk = pl.tk;
-  p.units = (int)pl.units;
+  p.splits = pl.splits;
+  p.n_items = pl.items;
+  p.grid = pl.grid;
   char* base = static_cast<char*>(ws);
   p.err = reinterpret_cast<uint32_t*>(base + pl.L.err);
   p.anc = reinterpret_cast<uint64_t*>(base + pl.L.anc);
   p.seq_tiles = reinterpret_cast<int32_t*>(base + pl.L.seq_tiles);
-  p.seq_base = reinterpret_cast<int64_t*>(base + pl.L.seq_base);
   p.seq_kv_base = reinterpret_cast<int64_t*>(base + pl.L.seq_kv_base);
   p.part_lse = reinterpret_cast<float*>(base + pl.L.part_lse);
   p.part_o = reinterpret_cast<float*>(base + pl.L.part_o);
@@ -181,10 +216,17 @@ mla_status mla_verify_attn(const mla_verify_args* a, void* workspace, size_t ws_
   mla_status st = make_plan(a, num_splits, &pl);
   if (st != MLA_OK) return st;
   if (pl.noop) return MLA_OK;
+  st = validate_call(a);
+  if (st != MLA_OK) return st;
   st = check_ws(pl, workspace, ws_bytes);
   if (st != MLA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (pl.sm_count == 0 && device_sm_count(&pl.sm_count) != 0) return MLA_ERR_CUDA;
+  {
+    const int64_t cap = (pl.algo == MLA_ALGO_TC) ? tc_clusters_per_gpu(pl.sm_count) : simt_ctas_per_gpu(pl.sm_count);
+    pl.grid = (int)(pl.items < cap ? pl.items : cap);
+    if (pl.grid < 1) pl.grid = 1;
+  }
   const Params p = make_params(a, pl, workspace);
   if (launch_meta(p, pl.sm_count, nullptr, 0, nullptr, s) != cudaSuccess) return MLA_ERR_CUDA;
   if (a->profile_events && cudaEventRecord((cudaEvent_t)a->profile_events[0], s) != cudaSuccess)
@@ -193,7 +235,7 @@ mla_status mla_verify_attn(const mla_verify_args* a, void* workspace, size_t ws_
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   if (a->profile_events && cudaEventRecord((cudaEvent_t)a->profile_events[1], s) != cudaSuccess)
     return MLA_ERR_CUDA;
-  if (launch_combine(p, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (pl.splits > 1 && launch_combine(p, s) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }
 
@@ -203,6 +245,8 @@ mla_status mla_verify_build_meta(const mla_verify_args* a, void* workspace, size
   mla_status st = make_plan(a, 1, &pl);
   if (st != MLA_OK) return st;
   if (pl.noop) return MLA_OK;
+  st = validate_tables(a);
+  if (st != MLA_OK) return st;
   if (!anc || !slots || slots_capacity < 0) return MLA_ERR_INVALID_ARG;
   st = check_ws(pl, workspace, ws_bytes);
   if (st != MLA_OK) return st;

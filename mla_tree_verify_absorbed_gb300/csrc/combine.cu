@@ -1,12 +1,12 @@
 // LSE combine of split-KV pieces (flash-decoding merge).
 //
-// A row group whose KV range was cut across several work units has one
-// normalised partial output o_s and log-sum-exp lse_s per piece.  Exactly:
+// A row group whose KV range was cut into several chunks has one normalised
+// partial output o_s and log-sum-exp lse_s per non-empty chunk.  Exactly:
 //   lse = ln sum_s exp(lse_s),   out = sum_s exp(lse_s - lse) * o_s,
 // because each piece's softmax over its own tokens, reweighted by its share
-// of the total exponent mass, is the softmax over the union.  Row groups done
-// by a single piece were written directly by the attention kernel and are
-// skipped here.
+// of the total exponent mass, is the softmax over the union.  With one chunk
+// per row group the attention kernel wrote the results directly and this
+// kernel is not launched.
 #include "common.cuh"
 
 namespace mlav {
@@ -22,34 +22,32 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   const int b = (int)(gw / p.rows);
   const int row = (int)(gw % p.rows);
   const int g = row / p.rg;
-  const int T = p.seq_tiles[b];
-  const int64_t W = p.seq_base[p.B];
-  const int64_t U = p.units;
-  const int64_t start = p.seq_base[b] + (int64_t)g * T;
-  const int64_t c0 = unit_of(start, W, U);
-  const int64_t c1 = unit_of(start + T - 1, W, U);
-  if (c0 == c1) return;  // written directly
-
+  const int64_t T = p.seq_tiles[b];
+  const int S = p.splits;
   const int r = row - g * p.rg;
+  auto item_of = [&](int k) { return ((int64_t)b * S + k) * p.groups + g; };
+  auto nonempty = [&](int k) { return ((int64_t)(k + 1) * T) / S > ((int64_t)k * T) / S; };
   float M = -INFINITY;
-  for (int64_t c = c0; c <= c1; ++c) M = fmaxf(M, p.part_lse[part_slot(c, b, g, p.groups) * p.rg + r]);
+  for (int k = 0; k < S; ++k)
+    if (nonempty(k)) M = fmaxf(M, p.part_lse[item_of(k) * p.rg + r]);
   float L = 0.f;
   float4 acc[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != -INFINITY) {
-    for (int64_t c = c0; c <= c1; ++c) {
-      const int64_t prow = part_slot(c, b, g, p.groups) * p.rg + r;
+    for (int k = 0; k < S; ++k) {
+      if (!nonempty(k)) continue;
+      const int64_t prow = item_of(k) * p.rg + r;
       const float w = __expf(p.part_lse[prow] - M);
       L += w;
       const float4* o = reinterpret_cast<const float4*>(p.part_o + prow * kDl);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float4 v = o[lane + 32 * k];
-        acc[k].x = fmaf(w, v.x, acc[k].x);
-        acc[k].y = fmaf(w, v.y, acc[k].y);
-        acc[k].z = fmaf(w, v.z, acc[k].z);
-        acc[k].w = fmaf(w, v.w, acc[k].w);
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = o[lane + 32 * q];
+        acc[q].x = fmaf(w, v.x, acc[q].x);
+        acc[q].y = fmaf(w, v.y, acc[q].y);
+        acc[q].z = fmaf(w, v.z, acc[q].z);
+        acc[q].w = fmaf(w, v.w, acc[q].w);
       }
     }
   }

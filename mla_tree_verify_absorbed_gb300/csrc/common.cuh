@@ -1,6 +1,6 @@
 // Shared device-side definitions of the verify-attention kernels: the launch
-// parameter block, the workspace layout, slot resolution, and the linear
-// work partition that the attention and combine kernels agree on.
+// parameter block, the workspace layout, slot resolution, and the work-item
+// partition that the attention and combine kernels agree on.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -37,27 +37,31 @@ struct Params {
   void* out;
   float* lse;
 
-  // partition
+  // partition: work item i = (b * splits + k) * groups + g covers row group g
+  // of sequence b over KV chunk k (tiles [k*T_b/splits, (k+1)*T_b/splits)).
+  // Chunk-major order puts the row groups of one chunk next to each other, so
+  // items running at the same time read the same KV from L2.
   int rg;            // rows per row group
   int groups;        // G = ceil(rows / rg)
   int tk;            // tokens per tile
-  int units;         // U: work units the linear tile space is cut into
+  int splits;        // S: KV chunks per row group
+  int64_t n_items;   // B * S * G
+  int grid;          // CTAs (or clusters) taking items round-robin
 
   // workspace views
   uint32_t* err;
   uint64_t* anc;           // [B][Q]
   int32_t* seq_tiles;      // [B]   T_b = ceil(N_b / tk)
-  int64_t* seq_base;       // [B+1] cumulative G * T_b  (linear work positions)
   int64_t* seq_kv_base;    // [B+1] cumulative N_b
-  float* part_lse;         // [slots][rg]  (natural log)
-  float* part_o;           // [slots][rg][512], normalised partial outputs
+  float* part_lse;         // [n_items][rg]  (natural log)
+  float* part_o;           // [n_items][rg][512], normalised partial outputs
 };
 
 // ---------------------------------------------------------------------------
 // Workspace layout: fixed regions, each 256-byte aligned.
 // ---------------------------------------------------------------------------
 struct WsLayout {
-  size_t err, anc, seq_tiles, seq_base, seq_kv_base, part_lse, part_o, total;
+  size_t err, anc, seq_tiles, seq_kv_base, part_lse, part_o, total;
   int64_t part_slots;
 };
 
@@ -69,7 +73,6 @@ inline WsLayout ws_layout(int B, int Q, int rg, int64_t part_slots) {
   L.err = o;          o = align256(o + 16);
   L.anc = o;          o = align256(o + sizeof(uint64_t) * (size_t)B * (size_t)Q + 8);
   L.seq_tiles = o;    o = align256(o + sizeof(int32_t) * (size_t)B + 4);
-  L.seq_base = o;     o = align256(o + sizeof(int64_t) * ((size_t)B + 1));
   L.seq_kv_base = o;  o = align256(o + sizeof(int64_t) * ((size_t)B + 1));
   L.part_lse = o;     o = align256(o + sizeof(float) * (size_t)part_slots * rg);
   L.part_o = o;       o = align256(o + sizeof(float) * (size_t)part_slots * rg * kDl);
@@ -104,53 +107,32 @@ __device__ __forceinline__ float load_elem(const void* base, int dtype, int64_t 
   return reinterpret_cast<const float*>(base)[idx];
 }
 
-// Linear work space: position x in [0, W) with W = seq_base[B]; sequence b
-// owns [seq_base[b], seq_base[b+1]) = G row groups x T_b tiles, row-group
-// major.  Unit c owns [floor(c*W/U), floor((c+1)*W/U)).
-__device__ __forceinline__ int64_t unit_lo(int64_t c, int64_t W, int64_t U) { return (c * W) / U; }
+// One work item: row group g of sequence b over KV tiles [t0, t1).
+struct Item {
+  int b, g, k;
+  int t0, t1;
+};
 
-// The unit whose range contains position x (W >= 1).
-__device__ __forceinline__ int64_t unit_of(int64_t x, int64_t W, int64_t U) {
-  return ((x + 1) * U - 1) / W;
+__device__ __forceinline__ Item item_at(const Params& p, int64_t i) {
+  Item it;
+  it.g = (int)(i % p.groups);
+  const int64_t bk = i / p.groups;
+  it.k = (int)(bk % p.splits);
+  it.b = (int)(bk / p.splits);
+  const int64_t T = p.seq_tiles[it.b];
+  it.t0 = (int)((it.k * T) / p.splits);
+  it.t1 = (int)(((it.k + 1) * T) / p.splits);
+  return it;
 }
 
-// Sequence owning linear position x (binary search over seq_base).
-__device__ __forceinline__ int seq_of(const int64_t* seq_base, int B, int64_t x) {
+// Sequence owning flat position k of the per-sequence prefix sums `base`.
+__device__ __forceinline__ int seq_of(const int64_t* base, int B, int64_t k) {
   int lo = 0, hi = B - 1;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
-    if (seq_base[mid] <= x) lo = mid; else hi = mid - 1;
+    if (base[mid] <= k) lo = mid; else hi = mid - 1;
   }
   return lo;
-}
-
-// Partial-output slot of unit c's piece of row group (b, g).  Units meeting a
-// row group are consecutive, so c + (b*G + g) never collides; it stays below
-// U + B*G.
-__device__ __forceinline__ int64_t part_slot(int64_t c, int b, int g, int G) {
-  return c + (int64_t)b * G + g;
-}
-
-// One contiguous piece of a unit's range inside one row group.
-struct Segment {
-  int b, g;
-  int t0, t1;      // tiles [t0, t1) of sequence b
-  int T;           // T_b
-  bool whole;      // the piece is the row group's whole KV range
-};
-
-__device__ __forceinline__ Segment segment_at(const Params& p, int64_t x, int64_t hi) {
-  Segment s;
-  s.b = seq_of(p.seq_base, p.B, x);
-  s.T = p.seq_tiles[s.b];
-  int64_t off = x - p.seq_base[s.b];
-  s.g = (int)(off / s.T);
-  s.t0 = (int)(off % s.T);
-  int64_t group_end = p.seq_base[s.b] + (int64_t)(s.g + 1) * s.T;
-  int64_t end = hi < group_end ? hi : group_end;
-  s.t1 = s.t0 + (int)(end - x);
-  s.whole = (s.t0 == 0 && s.t1 == s.T);
-  return s;
 }
 
 // bf16 / fp32 store of one output element.

@@ -1,6 +1,6 @@
 // Metadata kernels: ancestor-or-self masks of every draft tree, per-sequence
-// tile counts and their prefix sums (the linear work space the attention
-// kernels partition), and validation of every device-resident table entry.
+// tile counts (which the work items of the attention kernels cut into
+// chunks), and validation of every device-resident table entry.
 //
 // The mask rule follows "Reading the Reference: How a Single File-Read Message
 // Anchored a Complex CUDA Kernel Implementation", section "Output Knowledge
@@ -33,23 +33,21 @@ __device__ int64_t block_inclusive_scan(int64_t v, int64_t* sh) {
 
 // One block.  Clears the error word, validates prefix_lens / kv_indptr /
 // page capacity / parents, builds anc, T_b = ceil(N_b / tk), and the prefix
-// sums seq_base (G * T_b) and seq_kv_base (N_b).
+// sums seq_kv_base of N_b.
 __global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
   __shared__ int64_t sh[kMetaThreads];
-  __shared__ int64_t carry_work, carry_kv;
+  __shared__ int64_t carry_kv;
   const int tid = threadIdx.x;
   if (tid == 0) {
     *p.err = 0u;
-    carry_work = 0;
     carry_kv = 0;
-    p.seq_base[0] = 0;
     p.seq_kv_base[0] = 0;
   }
   __syncthreads();
 
   for (int b0 = 0; b0 < p.B; b0 += kMetaThreads) {
     const int b = b0 + tid;
-    int64_t work = 0, nkv = 0;
+    int64_t nkv = 0;
     if (b < p.B) {
       int64_t P = p.prefix_lens[b];
       uint32_t e = 0;
@@ -75,18 +73,14 @@ __global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
       if (e) set_err(p.err, e);
       const int64_t T = (N + p.tk - 1) / p.tk;
       p.seq_tiles[b] = (int32_t)T;
-      work = T * p.groups;
       nkv = N;
     }
-    const int64_t w_inc = block_inclusive_scan(work, sh);
     const int64_t k_inc = block_inclusive_scan(nkv, sh);
     if (b < p.B) {
-      p.seq_base[b + 1] = carry_work + w_inc;
       p.seq_kv_base[b + 1] = carry_kv + k_inc;
     }
     __syncthreads();
     if (tid == kMetaThreads - 1) {
-      carry_work += w_inc;
       carry_kv += k_inc;
     }
     __syncthreads();

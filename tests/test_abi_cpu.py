@@ -72,6 +72,14 @@ def attn(lib, a, ws=0x100000, nbytes=1 << 40, splits=1):
     ("Q", 65, api.MLA_ERR_UNSUPPORTED),
     ("dtype", 7, api.MLA_ERR_INVALID_ARG),
     ("algo", 9, api.MLA_ERR_INVALID_ARG),
+])
+def test_shape_validation(lib, field, value, status):
+    a = fake_args(**{field: value})
+    assert attn(lib, a) == status
+    assert lib.mla_verify_workspace_size(ctypes.byref(a), 1) == 0
+
+
+@pytest.mark.parametrize("field,value,status", [
     ("q_lat", None, api.MLA_ERR_INVALID_ARG),
     ("out", None, api.MLA_ERR_INVALID_ARG),
     ("kv_indices", None, api.MLA_ERR_INVALID_ARG),
@@ -83,10 +91,12 @@ def attn(lib, a, ws=0x100000, nbytes=1 << 40, splits=1):
     ("kv_c", 0x10008, api.MLA_ERR_INVALID_ARG),         # not 16-byte aligned
     ("scale", float("nan"), api.MLA_ERR_INVALID_ARG),
 ])
-def test_host_validation(lib, field, value, status):
+def test_call_validation(lib, field, value, status):
+    # the workspace size depends on shapes only; the call itself rejects these
     a = fake_args(**{field: value})
     assert attn(lib, a) == status
-    assert lib.mla_verify_workspace_size(ctypes.byref(a), 1) == 0
+    assert lib.mla_verify_workspace_size(ctypes.byref(a), 1) == \
+        lib.mla_verify_workspace_size(ctypes.byref(fake_args()), 1)
 
 
 def test_tc_requires_bf16(lib):
@@ -114,11 +124,13 @@ def test_workspace_checks(lib):
     assert attn(lib, a, ws=0) == api.MLA_ERR_WORKSPACE
     assert attn(lib, a, ws=0x100010) == api.MLA_ERR_WORKSPACE          # not 256-byte aligned
     assert attn(lib, a, nbytes=need - 1) == api.MLA_ERR_WORKSPACE
-    # more splits never need less workspace; both kernel families size it
-    assert lib.mla_verify_workspace_size(ctypes.byref(a), 4) >= need
+    # more splits never need less workspace; one split needs no partials
+    assert lib.mla_verify_workspace_size(ctypes.byref(a), 4) > need
+    assert lib.mla_verify_workspace_size(ctypes.byref(a), 4) >= 4 * 2 * 8 * 16 * 513 * 4
     b = fake_args(algo=api.ALGO["tc"])
     assert lib.mla_verify_workspace_size(ctypes.byref(b), 3) > 0
     assert lib.mla_verify_workspace_size(ctypes.byref(a), -1) == 0
+    assert lib.mla_verify_workspace_size(ctypes.byref(a), 5000) == 0
 
 
 def test_build_meta_validation(lib):
