@@ -293,6 +293,9 @@ def run_ours(args):
     # --- device-resident timed region ---------------------------------------
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
+    for a, b in evs:  # torch creates the CUDA event on first record
+        a.record(stream)
+        b.record(stream)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(physical_gpu_index(local)) if rank == 0 else None
     if sampler:
@@ -324,7 +327,7 @@ def run_ours(args):
     us_call = ms_step * 1000.0 / world
     kernel_s = attn_avg_ms / 1000.0
     eff_kv_gbs = cnt["kv_bytes"] / (ms_step / 1000.0) / 1e9
-    resolved = "tc" if (algo == "tc" or (algo == "auto" and tc_is_default())) else "simt"
+    resolved = "simt" if algo == "simt" else "tc"   # AUTO takes the tensor-core kernel for bf16
     if resolved == "tc":
         peak, src = peak_bf16_tflops()
         achieved = cnt["flops"] / kernel_s / 1e12
@@ -368,25 +371,6 @@ def run_ours(args):
         line["cpu_baseline"] = cpu_baseline(p)
     print(json.dumps(line), flush=True)
     return 0
-
-
-def tc_is_default() -> bool:
-    """Whether AUTO picks the tensor-core kernel for bf16 (asks the library)."""
-    import ctypes
-    from mla_tree_verify_absorbed_gb300 import api
-    a = api.MlaVerifyArgs()
-    a.B, a.Q, a.H, a.dtype = 1, 1, 128, api.MLA_BF16
-    p = 0x10000
-    for f in ("q_lat", "q_pe", "kv_c", "k_pe", "kv_indptr", "kv_indices", "prefix_lens",
-              "tree_parent", "out"):
-        setattr(a, f, p)
-        p += 0x10000
-    a.kv_c_stride, a.k_pe_stride, a.pool_slots, a.page_size, a.scale = 576, 576, 16, 1, 0.1
-    a.algo = api.ALGO["auto"]
-    n_auto = api.load().mla_verify_workspace_size(ctypes.byref(a), 1)
-    a.algo = api.ALGO["tc"]
-    n_tc = api.load().mla_verify_workspace_size(ctypes.byref(a), 1)
-    return n_auto == n_tc
 
 
 def run_e2e(args, p, di, dev, stream, algo, dist):
@@ -437,8 +421,8 @@ def run_e2e(args, p, di, dev, stream, algo, dist):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD, choices=list(I.CONFIG_NAMES))
     ap.add_argument("--num-splits", type=int, default=0)

@@ -156,6 +156,7 @@ mla_status mla_verify_check(const void *workspace, mla_stream_t stream, uint32_t
 #define MLA_DEVERR_PAGES 0x10u   /* sequence longer than max_pages * page_size */
 #define MLA_DEVERR_CAPACITY 0x20u/* build_meta: slots_capacity too small */
 #define MLA_DEVERR_TIMEOUT 0x40u /* a bounded device wait gave up */
+#define MLA_DEVERR_LAYOUT 0x80u  /* the tensor-core kernel's shared memory was not 1024-byte aligned */
 
 /* Human-readable name of a status code (static storage). */
 const char *mla_status_str(mla_status s);

@@ -23,7 +23,7 @@ ALGO = {"auto": 0, "simt": 1, "tc": 2}
 
 DEVERR = {
     0x1: "PREFIX", 0x2: "INDPTR", 0x4: "SLOT", 0x8: "PARENT", 0x10: "PAGES",
-    0x20: "CAPACITY", 0x40: "TIMEOUT",
+    0x20: "CAPACITY", 0x40: "TIMEOUT", 0x80: "LAYOUT",
 }
 
 # every symbol include/mla_verify.h declares

@@ -96,10 +96,12 @@ struct alignas(16) Ctl {
   uint64_t drain;           // both: final MMA drain on abort
   float alpha[2][kRG];      // value: per-row rescale of O before PV(j)
   int flag[2];              // value: some row of tile j rescaled
-  float lfin[kRG];          // value: final row sums (base-2 domain)
+  float lfin[kRG];          // value: final row sums of the bf16-rounded p (normalises out)
+  float lxfin[kRG];         // value: final row sums of the unrounded p (gives lse)
   float mfin[kRG];          // value: final running max (base-2 units)
   uint32_t tmem_base;
   int abort;
+  int abort_site;
   int cmd;
   int cmd_buf;
   long long cmd_item;
@@ -109,8 +111,18 @@ constexpr int kSmemAlloc = 232448;  // the per-CTA maximum; the base must be 102
 static_assert(kSmemBytes <= kSmemAlloc, "shared memory budget");
 static_assert(kOffKpe + kStages * (int)kKpeBytes <= kOffCtl, "k_pe stages overlap control block");
 
-__device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, Ctl* c, bool cluster = false) {
-  return mbar_wait(bar, parity, &c->abort, kWaitLimitNs, cluster);
+// Wait sites, recorded in the workspace's second error word when a wait gives up.
+enum {
+  kSiteEmpty = 1, kSiteQReady, kSiteFullS, kSiteSFree, kSiteSFull, kSitePFree, kSiteFinFree,
+  kSiteFullV, kSitePFull, kSitePvPrev, kSiteCmdDone, kSitePvLast, kSiteRelease, kSiteCmdFull, kSiteFinFull
+};
+
+__device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, Ctl* c, int site, int j,
+                                     bool cluster = false) {
+  if (mbar_wait(bar, parity, &c->abort, kWaitLimitNs, cluster)) return true;
+  // first site to give up in this CTA (others follow the abort flag)
+  atomicCAS(&c->abort_site, 0, (site & 0xff) | ((j & 0xffff) << 16));
+  return false;
 }
 
 __device__ __forceinline__ void red_or_cluster(uint32_t caddr, uint32_t v) {
@@ -149,7 +161,7 @@ __device__ void score_producer(const Params& p, const CUtensorMap* map_kvc, cons
       const uint32_t ph = (uint32_t)(j / kStages) & 1u;
       bool ok = true;
       if (lane == 0) {
-        ok = wait(&c->empty[s], ph ^ 1u, c, true);
+        ok = wait(&c->empty[s], ph ^ 1u, c, kSiteEmpty, j, true);
         if (ok) mbar_arrive_expect_tx(&c->full[s], kKvcBytes + kKpeBytes);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -174,7 +186,7 @@ __device__ void score_producer(const Params& p, const CUtensorMap* map_kvc, cons
   // drain: the last stages' copies must land before this CTA may exit
   if (lane == 0 && c->abort) {
     for (int q = j - kStages; q < j; ++q)
-      if (q >= 0) mbar_wait(&c->full[q % kStages], (uint32_t)(q / kStages) & 1u, &c->abort, kDrainLimitNs);
+      if (q >= 0) mbar_wait_drain(&c->full[q % kStages], (uint32_t)(q / kStages) & 1u, kDrainLimitNs);
   }
 }
 
@@ -185,22 +197,23 @@ __device__ void score_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id
   for (int64_t item = cluster_id; item < p.n_items; item += n_clusters) {
     const Item it = item_at(p, item);
     if (it.t1 <= it.t0) continue;
-    if (!wait(&c->q_ready, (uint32_t)seg & 1u, c)) return;
+    if (!wait(&c->q_ready, (uint32_t)seg & 1u, c, kSiteQReady, j)) return;
     tc_fence_after();
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       const int s = j % kStages, sb = j & 1;
-      if (!wait(&c->full[s], (uint32_t)(j / kStages) & 1u, c)) return;
-      if (!wait(&c->s_free[sb], ((uint32_t)(j >> 1) & 1u) ^ 1u, c)) return;
+      if (!wait(&c->full[s], (uint32_t)(j / kStages) & 1u, c, kSiteFullS, j)) return;
+      if (!wait(&c->s_free[sb], ((uint32_t)(j >> 1) & 1u) ^ 1u, c, kSiteSFree, j)) return;
       tc_fence_after();
-      const uint32_t kvc = smem_u32(smem + kOffKvc + s * kKvcStage);
-      const uint32_t kpe = smem_u32(smem + kOffKpe + s * kKpeBytes);
-#pragma unroll 1
+      // descriptors differ only in the start-address field: add (offset >> 4)
+      const uint64_t dk = smem_desc(smem_u32(smem + kOffKvc + s * kKvcStage), 16, 1024, kLayoutSw128);
+      const uint64_t dp = smem_desc(smem_u32(smem + kOffKpe + s * kKpeBytes), 16, 1024, kLayoutSw128);
+      const uint32_t ts = tS + sb * kTK;
+#pragma unroll
       for (int kc = 0; kc < 9; ++kc) {
-        const uint32_t base = kc < 8 ? kvc + kc * kChunk : kpe;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bd = smem_desc(base + kk * 32, 16, 1024, kLayoutSw128);
-          mma_ts(tS + sb * kTK, tQ + kc * 32 + kk * 8, bd, kIdescS, (kc | kk) != 0);
+          const uint64_t bd = (kc < 8 ? dk + (uint64_t)((kc * kChunk + kk * 32) >> 4) : dp + (uint64_t)((kk * 32) >> 4));
+          mma_ts(ts, tQ + kc * 32 + kk * 8, bd, kIdescS, (kc | kk) != 0);
         }
       }
       mma_commit(&c->s_full[sb]);
@@ -229,6 +242,7 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
 
     // stage this item's queries into TMEM: column c holds elements 2c, 2c+1
     {
+      __syncwarp();
       const uint4* ql = reinterpret_cast<const uint4*>(p.q_lat) + ((int64_t)b * p.rows + row) * (kDl / 8);
       const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe) + ((int64_t)b * p.rows + row) * (kDr / 8);
 #pragma unroll 1
@@ -244,6 +258,7 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
           w[4 * v + 2] = x.z;
           w[4 * v + 3] = x.w;
         }
+        __syncwarp();
         tmem_st_32x32b_x32(tQ + c0, w);
       }
       tmem_wait_st();
@@ -251,10 +266,13 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
       mbar_arrive(&c->q_ready);
     }
 
-    float m = -INFINITY, l = 0.f;
+    // l sums the bf16-rounded weights the value CTA multiplies by, so out is
+    // normalised consistently; lx sums the unrounded weights for an exact lse
+    float m = -INFINITY, l = 0.f, lx = 0.f;
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       const int sb = j & 1;
-      if (!wait(&c->s_full[sb], (uint32_t)(j >> 1) & 1u, c)) return;
+      if (!wait(&c->s_full[sb], (uint32_t)(j >> 1) & 1u, c, kSiteSFull, j)) return;
+      __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the spin
       tc_fence_after();
       float x[kTK];
       {
@@ -296,18 +314,22 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
       if (need) {
         alpha = exp2f(m - tmax);  // 0 when m is -inf
         l *= alpha;
+        lx *= alpha;
         m = tmax;
       }
       const float mu = (m == -INFINITY) ? 0.f : m;
 
       // wait until the value CTA is done with this P buffer
-      if (!wait(&c->p_free[sb], ((uint32_t)(j >> 1) & 1u) ^ 1u, c, true)) return;
+      if (!wait(&c->p_free[sb], ((uint32_t)(j >> 1) & 1u) ^ 1u, c, kSitePFree, j, true)) return;
       const uint32_t pbase = mapa_shared(smem_u32(smem + kOffP + sb * kPBytes), 1);
 #pragma unroll
       for (int q8 = 0; q8 < 8; ++q8) {
         float e[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) e[u] = exp2f(x[8 * q8 + u] - mu);
+        for (int u = 0; u < 8; ++u) {
+          e[u] = exp2f(x[8 * q8 + u] - mu);
+          lx += e[u];
+        }
         const uint32_t w0 = pack_bf16(e[0], e[1]), w1 = pack_bf16(e[2], e[3]);
         const uint32_t w2 = pack_bf16(e[4], e[5]), w3 = pack_bf16(e[6], e[7]);
         // the row sum uses the rounded values the value CTA multiplies by
@@ -331,8 +353,9 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
     }
 
     // hand the row statistics to the value CTA for the epilogue
-    if (!wait(&c->fin_free, ((uint32_t)seg & 1u) ^ 1u, c, true)) return;
+    if (!wait(&c->fin_free, ((uint32_t)seg & 1u) ^ 1u, c, kSiteFinFree, j, true)) return;
     st_cluster_f32(mapa_shared(smem_u32(&c->lfin[r]), 1), l);
+    st_cluster_f32(mapa_shared(smem_u32(&c->lxfin[r]), 1), lx);
     st_cluster_f32(mapa_shared(smem_u32(&c->mfin[r]), 1), m);
     mbar_arrive_cluster(&c->fin_full, 1);
     ++seg;
@@ -352,42 +375,41 @@ __device__ void value_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       const int s = j % kStages, pb = j & 1;
       mbar_arrive_expect_tx(&c->full[s], kKvcBytes);
-      if (!(ok = wait(&c->full[s], (uint32_t)(j / kStages) & 1u, c))) break;
-      if (!(ok = wait(&c->p_full[pb], (uint32_t)(j >> 1) & 1u, c, true))) break;
+      if (!(ok = wait(&c->full[s], (uint32_t)(j / kStages) & 1u, c, kSiteFullV, j))) break;
+      if (!(ok = wait(&c->p_full[pb], (uint32_t)(j >> 1) & 1u, c, kSitePFull, j, true))) break;
       const bool first = (t == it.t0);
       if (!first && c->flag[pb]) {
         // O must hold PV(j-1) in full before it is rescaled
-        if (!(ok = wait(&c->pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c))) break;
+        if (!(ok = wait(&c->pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c, kSitePvPrev, j))) break;
         tc_fence_after();
         c->cmd = kCmdRescale;
         c->cmd_buf = pb;
         mbar_arrive(&c->cmd_full);
-        if (!(ok = wait(&c->cmd_done, (uint32_t)ncmd & 1u, c))) break;
+        if (!(ok = wait(&c->cmd_done, (uint32_t)ncmd & 1u, c, kSiteCmdDone, j))) break;
         ++ncmd;
       }
       tc_fence_after();
-      const uint32_t pa = smem_u32(smem + kOffP + pb * kPBytes);
-      const uint32_t kvc = smem_u32(smem + kOffKvc + s * kKvcStage);
+      const uint64_t da = smem_desc(smem_u32(smem + kOffP + pb * kPBytes), 16, 1024, kLayoutSw128);
+      const uint64_t dv = smem_desc(smem_u32(smem + kOffKvc + s * kKvcStage), MLA_TC_V_LBO, MLA_TC_V_SBO,
+                                    kLayoutSw128);
 #pragma unroll
-      for (int nh = 0; nh < 2; ++nh) {
+      for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ad = smem_desc(pa + kk * 32, 16, 1024, kLayoutSw128);
-          const uint64_t bd = smem_desc(kvc + nh * 4 * kChunk + kk * 16 * 128, MLA_TC_V_LBO, MLA_TC_V_SBO,
-                                        kLayoutSw128);
-          mma_ss(tO + nh * 256, ad, bd, kIdescPV, !(first && kk == 0));
+        for (int nh = 0; nh < 2; ++nh) {
+          mma_ss(tO + nh * 256, da + (uint64_t)((kk * 32) >> 4),
+                 dv + (uint64_t)((nh * 4 * kChunk + kk * 16 * 128) >> 4), kIdescPV, !(first && kk == 0));
         }
       }
       mma_commit(&c->pv_done[pb]);
     }
     if (!ok) break;
     // epilogue of this item once its last PV is complete
-    if (!(ok = wait(&c->pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c))) break;
+    if (!(ok = wait(&c->pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c, kSitePvLast, j))) break;
     tc_fence_after();
     c->cmd = kCmdEpilogue;
     c->cmd_item = item;
     mbar_arrive(&c->cmd_full);
-    if (!(ok = wait(&c->cmd_done, (uint32_t)ncmd & 1u, c))) break;
+    if (!(ok = wait(&c->cmd_done, (uint32_t)ncmd & 1u, c, kSiteCmdDone, j))) break;
     ++ncmd;
     ++seg;
   }
@@ -396,9 +418,9 @@ __device__ void value_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id
   if (c->abort) {
     // drain: outstanding MMAs and multicast copies into this CTA
     mma_commit(&c->drain);
-    mbar_wait(&c->drain, 0, &c->abort, kDrainLimitNs);
+    mbar_wait_drain(&c->drain, 0, kDrainLimitNs);
     for (int q = j - kStages + 1; q <= j; ++q)
-      if (q >= 0) mbar_wait(&c->full[q % kStages], (uint32_t)(q / kStages) & 1u, &c->abort, kDrainLimitNs);
+      if (q >= 0) mbar_wait_drain(&c->full[q % kStages], (uint32_t)(q / kStages) & 1u, kDrainLimitNs);
   }
 }
 
@@ -409,7 +431,7 @@ __device__ void value_release(const Params& p, Ctl* c, int cluster_id, int n_clu
   for (int64_t item = cluster_id; item < p.n_items; item += n_clusters) {
     const Item it = item_at(p, item);
     for (int t = it.t0; t < it.t1; ++t, ++j) {
-      if (!wait(&c->pv_done[j & 1], (uint32_t)(j >> 1) & 1u, c)) return;
+      if (!wait(&c->pv_done[j & 1], (uint32_t)(j >> 1) & 1u, c, kSiteRelease, j)) return;
       c->flag[j & 1] = 0;  // ordered before the release below
       mbar_arrive_cluster(&c->empty[j % kStages], 0);
       mbar_arrive_cluster(&c->p_free[j & 1], 0);
@@ -424,43 +446,46 @@ __device__ void value_epilogue(const Params& p, Ctl* c) {
   int ncmd = 0, seg = 0;
   const float ln2 = 0.69314718055994530942f;
   while (true) {
-    if (!wait(&c->cmd_full, (uint32_t)ncmd & 1u, c)) return;
+    if (!wait(&c->cmd_full, (uint32_t)ncmd & 1u, c, kSiteCmdFull, ncmd)) return;
+    __syncwarp();
     ++ncmd;
     const int cmd = c->cmd;
     if (cmd == kCmdExit) return;
     tc_fence_after();
     if (cmd == kCmdRescale) {
+      // warp-collective TMEM traffic: every row takes part (factor 1 = unchanged)
       const float a = c->alpha[c->cmd_buf][r];
-      if (a != 1.f) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < kDl; c0 += 32) {
-          uint32_t u[32];
-          tmem_ld_32x32b_x32(tO + c0, u);
-          tmem_wait_ld();
+      for (int c0 = 0; c0 < kDl; c0 += 32) {
+        uint32_t u[32];
+        tmem_ld_32x32b_x32(tO + c0, u);
+        tmem_wait_ld();
 #pragma unroll
-          for (int q = 0; q < 32; ++q) u[q] = __float_as_uint(__uint_as_float(u[q]) * a);
-          tmem_st_32x32b_x32(tO + c0, u);
-        }
-        tmem_wait_st();
+        for (int q = 0; q < 32; ++q) u[q] = __float_as_uint(__uint_as_float(u[q]) * a);
+        tmem_st_32x32b_x32(tO + c0, u);
       }
+      tmem_wait_st();
     } else {  // kCmdEpilogue
       const Item it = item_at(p, c->cmd_item);
-      if (!wait(&c->fin_full, (uint32_t)seg & 1u, c, true)) return;
-      const float l = c->lfin[r], m = c->mfin[r];
+      if (!wait(&c->fin_full, (uint32_t)seg & 1u, c, kSiteFinFull, seg, true)) return;
+      __syncwarp();
+      const float l = c->lfin[r], lx = c->lxfin[r], m = c->mfin[r];
       mbar_arrive_cluster(&c->fin_free, 0);
       ++seg;
       const int row = it.g * kRG + r;
-      if (row < p.rows) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const float lse = l > 0.f ? (m + log2f(l)) * ln2 : -INFINITY;
-        const int64_t orow = (int64_t)it.b * p.rows + row;
-        if (p.splits == 1) {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDl);
+      const bool live = row < p.rows;  // TMEM loads stay warp-wide; only stores are per row
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float lse = lx > 0.f ? (m + log2f(lx)) * ln2 : -INFINITY;
+      const int64_t orow = (int64_t)it.b * p.rows + row;
+      if (p.splits == 1) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDl);
 #pragma unroll 1
-          for (int c0 = 0; c0 < kDl; c0 += 32) {
-            uint32_t u[32];
-            tmem_ld_32x32b_x32(tO + c0, u);
-            tmem_wait_ld();
+        for (int c0 = 0; c0 < kDl; c0 += 32) {
+          uint32_t u[32];
+          __syncwarp();
+          tmem_ld_32x32b_x32(tO + c0, u);
+          tmem_wait_ld();
+          if (live) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               uint4 o;
@@ -471,22 +496,25 @@ __device__ void value_epilogue(const Params& p, Ctl* c) {
               dst[c0 / 8 + v] = o;
             }
           }
-          if (p.lse) p.lse[orow] = lse;
-        } else {
-          const int64_t prow = c->cmd_item * kRG + r;
-          float4* dst = reinterpret_cast<float4*>(p.part_o + prow * kDl);
+        }
+        if (live && p.lse) p.lse[orow] = lse;
+      } else {
+        const int64_t prow = c->cmd_item * kRG + r;
+        float4* dst = reinterpret_cast<float4*>(p.part_o + prow * kDl);
 #pragma unroll 1
-          for (int c0 = 0; c0 < kDl; c0 += 32) {
-            uint32_t u[32];
-            tmem_ld_32x32b_x32(tO + c0, u);
-            tmem_wait_ld();
+        for (int c0 = 0; c0 < kDl; c0 += 32) {
+          uint32_t u[32];
+          __syncwarp();
+          tmem_ld_32x32b_x32(tO + c0, u);
+          tmem_wait_ld();
+          if (live) {
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               dst[c0 / 4 + v] = make_float4(__uint_as_float(u[4 * v + 0]) * inv, __uint_as_float(u[4 * v + 1]) * inv,
                                             __uint_as_float(u[4 * v + 2]) * inv, __uint_as_float(u[4 * v + 3]) * inv);
           }
-          p.part_lse[prow] = lse;
         }
+        if (live) p.part_lse[prow] = lse;
       }
     }
     tc_fence_before();
@@ -501,9 +529,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw;
   const uint32_t rank = cluster_ctarank();
   const int warp = threadIdx.x >> 5;
-  // both CTAs see the same error word and the same alignment, so they agree
-  if (*p.err || (smem_u32(smem) & 1023u)) {
-    if (threadIdx.x == 0 && (smem_u32(smem) & 1023u)) set_err(p.err, MLA_DEVERR_TIMEOUT);
+  // Both CTAs of a cluster must take the same branch here.  The validation bits
+  // were final before this kernel started; the timeout bit may be raised by
+  // another cluster while this one starts, so it is not part of the test.
+  if ((*p.err & ~MLA_DEVERR_TIMEOUT) || (smem_u32(smem) & 1023u)) {
+    if (threadIdx.x == 0 && (smem_u32(smem) & 1023u)) set_err(p.err, MLA_DEVERR_LAYOUT);
     return;
   }
   Ctl* c = reinterpret_cast<Ctl*>(smem + kOffCtl);
@@ -527,6 +557,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&c->cmd_done, kRG);
     mbar_init(&c->drain, 1);
     c->abort = 0;
+    c->abort_site = 0;
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -559,10 +590,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (rank == 0 && threadIdx.x == 0 && c->abort) {
     // outstanding S MMAs must finish before TMEM is released
     mma_commit(&c->drain);
-    mbar_wait(&c->drain, 0, &c->abort, kDrainLimitNs);
+    mbar_wait_drain(&c->drain, 0, kDrainLimitNs);
   }
   if (threadIdx.x == 0 && c->abort) {
     set_err(p.err, MLA_DEVERR_TIMEOUT);
+    atomicCAS(p.err + 1, 0u, (uint32_t)c->abort_site | (rank << 8));
     // let multicast copies issued by the peer before it stopped land here
     const uint64_t t0 = globaltimer_ns();
     while (globaltimer_ns() - t0 < kDrainLimitNs) {

@@ -90,6 +90,7 @@ mla_status validate_call(const mla_verify_args* a) {
       !aligned16(a->out))
     return MLA_ERR_INVALID_ARG;
   if (!std::isfinite(a->scale)) return MLA_ERR_INVALID_ARG;
+  if (a->profile_events && (!a->profile_events[0] || !a->profile_events[1])) return MLA_ERR_INVALID_ARG;
   return MLA_OK;
 }
 

@@ -39,7 +39,8 @@ __global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
   __shared__ int64_t carry_kv;
   const int tid = threadIdx.x;
   if (tid == 0) {
-    *p.err = 0u;
+    p.err[0] = 0u;
+    p.err[1] = 0u;  // where a bounded wait gave up, if one did
     carry_kv = 0;
     p.seq_kv_base[0] = 0;
   }
