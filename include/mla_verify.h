@@ -132,6 +132,25 @@ size_t mla_verify_workspace_size(const mla_verify_args *args, int num_splits);
 mla_status mla_verify_attn(const mla_verify_args *args, void *workspace, size_t ws_bytes,
                            int num_splits, mla_stream_t stream);
 
+/* Same computation as mla_verify_attn, for callers that cannot allocate device
+ * memory when they make the call (a plugin inside an engine that owns the
+ * whole device memory pool, a decode loop that must not take the device-wide
+ * synchronisation of cudaMalloc) and so have no workspace to pass.  The pages
+ * have no counterpart of this entry point.
+ * It allocates nothing: its workspace is a fixed array of
+ * MLA_NOALLOC_SCRATCH_BYTES compiled into the library, held on every device
+ * that loads the library until the process exits.  Arguments, outputs and
+ * num_splits mean what they mean for mla_verify_attn; a call whose
+ * mla_verify_workspace_size exceeds MLA_NOALLOC_SCRATCH_BYTES returns
+ * MLA_ERR_WORKSPACE before launching anything (use fewer splits, or
+ * mla_verify_attn).  The first call on a device looks up the array's device
+ * address and caches it; make that first call before any stream capture.
+ * All calls share the array and it keeps the previous call's contents (the
+ * error word is cleared at the start of each call); calls that overlap on the
+ * GPU race on it, so order them on one stream. */
+#define MLA_NOALLOC_SCRATCH_BYTES (32u << 20)
+mla_status mla_verify_attn_noalloc(const mla_verify_args *args, int num_splits, mla_stream_t stream);
+
 /* Parity / debug export of the index work the attention kernels rely on.
  * Runs the metadata kernel and writes
  *   anc   [B][Q] uint64: bit t set when node t is node i or an ancestor of it;

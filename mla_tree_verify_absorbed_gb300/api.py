@@ -27,8 +27,9 @@ DEVERR = {
 }
 
 # every symbol include/mla_verify.h declares
-EXPORTS = ("mla_verify_workspace_size", "mla_verify_attn", "mla_verify_build_meta",
-           "mla_verify_check", "mla_status_str", "mla_verify_abi_version")
+EXPORTS = ("mla_verify_workspace_size", "mla_verify_attn", "mla_verify_attn_noalloc",
+           "mla_verify_build_meta", "mla_verify_check", "mla_status_str", "mla_verify_abi_version")
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class MlaVerifyArgs(ctypes.Structure):
@@ -73,6 +74,8 @@ def load(path: Optional[str] = None):
     lib.mla_verify_attn.restype = ctypes.c_int
     lib.mla_verify_attn.argtypes = [ctypes.POINTER(MlaVerifyArgs), ctypes.c_void_p, ctypes.c_size_t,
                                     ctypes.c_int, ctypes.c_void_p]
+    lib.mla_verify_attn_noalloc.restype = ctypes.c_int
+    lib.mla_verify_attn_noalloc.argtypes = [ctypes.POINTER(MlaVerifyArgs), ctypes.c_int, ctypes.c_void_p]
     lib.mla_verify_build_meta.restype = ctypes.c_int
     lib.mla_verify_build_meta.argtypes = [ctypes.POINTER(MlaVerifyArgs), ctypes.c_void_p, ctypes.c_size_t,
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
@@ -219,6 +222,25 @@ def verify_attn(di: DeviceInputs, out=None, lse=None, num_splits: int = 0, algo:
                              int(num_splits), _stream(stream))
     if st != MLA_OK:
         raise MlaError(st, "mla_verify_attn")
+    return out, lse
+
+
+def verify_attn_noalloc(di: DeviceInputs, out=None, lse=None, num_splits: int = 0, algo: str = "auto",
+                        stream=None):
+    """Run mla_verify_attn_noalloc (library-held scratch, no workspace); returns
+    (out, lse).  Output tensors are created here when not given -- the library
+    call itself allocates nothing."""
+    import torch
+    dev = di.q_lat.device
+    odt = torch.bfloat16 if di.dtype == "bf16" else torch.float32
+    if out is None:
+        out = torch.empty((di.B, di.Q, di.H, 512), dtype=odt, device=dev)
+    if lse is None:
+        lse = torch.empty((di.B, di.Q, di.H), dtype=torch.float32, device=dev)
+    a = make_args(di, out, lse, algo)
+    st = load().mla_verify_attn_noalloc(ctypes.byref(a), int(num_splits), _stream(stream))
+    if st != MLA_OK:
+        raise MlaError(st, "mla_verify_attn_noalloc")
     return out, lse
 
 
