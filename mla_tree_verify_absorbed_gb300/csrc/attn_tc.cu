@@ -1,5 +1,6 @@
 // Tensor-core split-KV verify attention for sm_103a: tcgen05 MMAs with TMEM
-// accumulators, TMA gathers of the paged KV, a 2-CTA cluster per work item.
+// accumulators, asynchronous gathers of the paged KV, a 2-CTA cluster per work
+// item.
 //
 // Shape of the problem.  Per work item, 128 query rows (absorbed queries of
 // (node, head) pairs; "Ground Truth in Silicon ...", section "Input Knowledge
@@ -21,24 +22,28 @@
 //   * the value CTA (rank 1) keeps O (512 columns) in TMEM and runs
 //     O += P.V (SS form, M=128, N=256 twice, K=64), with V read straight out
 //     of the staged kv_c tile as an MN-major operand.
-// P (bf16) travels from the score CTA's registers into the value CTA's
-// shared memory through distributed shared memory; the rare rescale factors
-// ride along.  The value CTA also writes the outputs.
+// P (bf16) and the per-row rescale factors travel from the score CTA's
+// registers into the value CTA's shared memory as st.async stores whose bytes
+// complete the value CTA's barrier.  The value CTA also writes the outputs.
 //
-// Data movement.  A producer warp in the score CTA gathers each 64-token tile
-// with TMA tile::gather4 (four pool rows per instruction, 128-byte swizzle,
-// 64-column boxes), kv_c multicast to both CTAs of the cluster, k_pe to the
-// score CTA only; three stages in flight.  Each staged tile is reused by all
-// 128 rows of the item -- the head-tile reuse of "The Critical Glue:
-// Validating a Custom Flash Attention Kernel Through Test Infrastructure",
-// section "What Came Before", widened to every (node, head) row.
+// Data movement.  Each CTA stages its own 64-token KV tiles, three in flight:
+// eight producer warps gather every token's pool row (kv_c, and k_pe in the
+// score CTA) with 16-byte cp.async copies written straight into the 128-byte
+// swizzled K-major layout the MMAs read, one 1 KB kv_c row per warp
+// instruction pair so each instruction reads 512 contiguous bytes; slot
+// indices are fetched one tile ahead.  Measured on GB300, the rate at which
+// one SM can gather scattered rows grows with the number of warps issuing
+// copies (outstanding requests per warp are limited): about 9 B/clk with two
+// warps and 50 B/clk with eight when the rows sit in L2; a TMA tile::gather4
+// version (four 128-byte rows per instruction) managed about 7 B/clk.  L2
+// bandwidth is ample, so each CTA loading its own copy costs nothing that
+// matters.  Each staged tile is reused by all 128 rows of the item -- the
+// head-tile reuse of "The Critical Glue: Validating a Custom Flash Attention
+// Kernel Through Test Infrastructure", section "What Came Before", widened to
+// every (node, head) row.
 //
 // Every wait is bounded; on timeout the kernel sets MLA_DEVERR_TIMEOUT, stops
 // issuing work, drains what it issued, frees TMEM and returns.
-#include <mutex>
-
-#include <cudaTypedefs.h>
-
 #include "common.cuh"
 #include "sm100.cuh"
 
@@ -50,27 +55,29 @@ namespace tc {
 constexpr int kRG = 128;        // query rows per work item (MMA M)
 constexpr int kTK = 64;         // tokens per KV tile
 constexpr int kStages = 3;      // KV tiles in flight
-constexpr int kThreads = 256;   // 8 warps
+constexpr int kThreads = 512;   // 16 warps
 constexpr uint32_t kTmemCols = 512;
+
+// warp roles
+constexpr int kProducerWarps = 8;                  // warps 0-7
+constexpr int kProducerThreads = 32 * kProducerWarps;
+constexpr int kTokPerWarp = kTK / kProducerWarps;  // 8 tokens of each tile per producer warp
+constexpr int kWarpMma = 8, kWarpRelease = 9, kWarpTmem = 10, kWarpRows = 12;  // rows: 12-15
 
 constexpr int kChunk = kTK * 128;            // one 64-column bf16 chunk of a tile: 8 KB
 constexpr int kKvcStage = 8 * kChunk;        // kv_c of one tile: 64 KB
-constexpr int kOffKvc = 0;                   // [kStages][64 KB], same offset in both CTAs
+constexpr int kOffKvc = 0;                   // [kStages][64 KB]
 constexpr int kOffKpe = kStages * kKvcStage; // score CTA: [kStages][8 KB]
 constexpr int kOffP = kStages * kKvcStage;   // value CTA: [2][16 KB]
 constexpr int kPBytes = kRG * 128;           // P tile [128 rows x 64 tokens] bf16
 constexpr int kOffCtl = kStages * kKvcStage + 2 * kPBytes;
-constexpr uint32_t kKvcBytes = kTK * kDl * 2;  // 65536
-constexpr uint32_t kKpeBytes = kTK * kDr * 2;  // 8192
+constexpr uint32_t kKpeBytes = kTK * kDr * 2;      // 8192
+constexpr uint32_t kPTxBytes = kPBytes + kRG * 4;  // P tile + alpha, per tile
 
 // Byte strides of the MN-major V operand (tile chunk = 64 columns x 64 rows):
 // between 64-column atoms along N, and between 8-row groups along K.
 constexpr uint32_t kVAtomStrideN = kChunk;   // 8192
 constexpr uint32_t kVGroupStrideK = 1024;
-#ifndef MLA_TC_V_LBO
-#define MLA_TC_V_LBO kVAtomStrideN
-#define MLA_TC_V_SBO kVGroupStrideK
-#endif
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTK, 0, 0);   // A (Q, TMEM), B (K tile) K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);  // A (P) K-major, B (V) MN-major
@@ -81,21 +88,20 @@ constexpr uint64_t kDrainLimitNs = 20000000ull;   // 20 ms per drain wait on abo
 enum { kCmdRescale = 1, kCmdEpilogue = 2, kCmdExit = 3 };
 
 struct alignas(16) Ctl {
-  uint64_t full[kStages];   // KV tile landed (score: kv_c + k_pe, value: kv_c)
-  uint64_t empty[kStages];  // score: stage reusable (S MMA done + value CTA's PV done)
+  uint64_t full[kStages];   // KV tile landed (kProducerThreads cp.async arrivals)
+  uint64_t empty[kStages];  // stage reusable: the MMAs reading it are complete
   uint64_t s_full[2];       // score: S tile in TMEM
   uint64_t s_free[2];       // score: softmax has read S (128 arrivals)
   uint64_t p_free[2];       // score: value CTA finished with its P buffer
   uint64_t q_ready;         // score: queries staged in TMEM (128 arrivals)
   uint64_t fin_free;        // score: value CTA consumed lfin/mfin (128 remote arrivals)
-  uint64_t p_full[2];       // value: P, alpha and flag written (128 remote arrivals)
+  uint64_t p_full[2];       // value: P tile and alpha landed (st.async bytes; armed by the MMA thread)
   uint64_t pv_done[2];      // value: PV MMAs of a tile complete
   uint64_t fin_full;        // value: lfin/mfin written (128 remote arrivals)
   uint64_t cmd_full;        // value: a command for the epilogue warps
   uint64_t cmd_done;        // value: command finished (128 arrivals)
   uint64_t drain;           // both: final MMA drain on abort
-  float alpha[2][kRG];      // value: per-row rescale of O before PV(j)
-  int flag[2];              // value: some row of tile j rescaled
+  float alpha[2][kRG];      // value: per-row rescale of O before PV(j) (1 = unchanged)
   float lfin[kRG];          // value: final row sums of the bf16-rounded p (normalises out)
   float lxfin[kRG];         // value: final row sums of the unrounded p (gives lse)
   float mfin[kRG];          // value: final running max (base-2 units)
@@ -110,6 +116,7 @@ constexpr int kSmemBytes = kOffCtl + (int)sizeof(Ctl);
 constexpr int kSmemAlloc = 232448;  // the per-CTA maximum; the base must be 1024-aligned
 static_assert(kSmemBytes <= kSmemAlloc, "shared memory budget");
 static_assert(kOffKpe + kStages * (int)kKpeBytes <= kOffCtl, "k_pe stages overlap control block");
+static_assert(kWarpRows % 4 == 0, "the row warps must form a warpgroup (TMEM lane quadrants)");
 
 // Wait sites, recorded in the workspace's second error word when a wait gives up.
 enum {
@@ -125,19 +132,12 @@ __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, Ctl* c, int
   return false;
 }
 
-__device__ __forceinline__ void red_or_cluster(uint32_t caddr, uint32_t v) {
-  asm volatile("red.relaxed.cluster.shared::cluster.or.b32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void tma_gather4_mc(void* dst, const CUtensorMap* map, int32_t x, int32_t y0,
-                                               int32_t y1, int32_t y2, int32_t y3, uint64_t* bar,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
+// 2^x by the hardware approximation (flushes results below 2^-126 to zero,
+// which only drops weights negligible against the row max).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -146,50 +146,85 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 // ---------------------------------------------------------------------------
-// score CTA roles
+// producers (both CTAs)
 // ---------------------------------------------------------------------------
-__device__ void score_producer(const Params& p, const CUtensorMap* map_kvc, const CUtensorMap* map_kpe,
-                               uint8_t* smem, Ctl* c, int cluster_id, int n_clusters) {
+// Stages the KV tiles of this CTA's items.  Producer warp pw copies tokens
+// [8 pw, 8 pw + 8) of each tile: for every token, two warp instructions move
+// its 1 KB kv_c row (lane l moves bytes 16l.. of each half), placing 16-byte
+// piece q of 64-column chunk ch of token row r at
+//   ch * kChunk + r * 128 + ((q ^ (r & 7)) * 16)
+// -- the 128-byte swizzle of the K-major operand layout.  In the score CTA two
+// more instructions move the 128-byte k_pe rows (four tokens each).  Positions
+// past the sequence read slot 0; the softmax gives them zero weight.
+__device__ void producer(const Params& p, uint8_t* smem, Ctl* c, int pw, bool with_kpe, int cluster_id,
+                         int n_clusters) {
   const int lane = threadIdx.x & 31;
+  const __nv_bfloat16* kvc_g = reinterpret_cast<const __nv_bfloat16*>(p.kv_c);
+  const __nv_bfloat16* kpe_g = reinterpret_cast<const __nv_bfloat16*>(p.k_pe);
+  const uint32_t sbase = smem_u32(smem);
+  const int r0 = kTokPerWarp * pw;
   int j = 0;
   for (int64_t item = cluster_id; item < p.n_items; item += n_clusters) {
     const Item it = item_at(p, item);
+    if (it.t1 <= it.t0) continue;
     const int b = it.b;
     const int64_t N = (int64_t)p.prefix_lens[b] + p.Q;
+    const int64_t idx0 = p.page_size == 1 ? (int64_t)p.kv_indptr[b] : 0;
+    // slot of token r0 + (lane % 8) of tile t
+    auto slot_of = [&](int t) -> int64_t {
+      const int64_t pos = (int64_t)t * kTK + r0 + (lane & (kTokPerWarp - 1));
+      if (pos >= N) return 0;
+      int64_t sl;
+      if (p.page_size == 1) {
+        sl = p.kv_indices[idx0 + pos];
+      } else {
+        sl = (int64_t)p.block_table[(int64_t)b * p.max_pages + pos / p.page_size] * p.page_size +
+             pos % p.page_size;
+      }
+      return (sl < 0 || sl >= p.pool_slots) ? 0 : sl;
+    };
+    int64_t next = slot_of(it.t0);
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       const int s = j % kStages;
-      const uint32_t ph = (uint32_t)(j / kStages) & 1u;
+      const int64_t slot = next;
+      if (t + 1 < it.t1) next = slot_of(t + 1);  // index load for the next tile, in flight meanwhile
       bool ok = true;
-      if (lane == 0) {
-        ok = wait(&c->empty[s], ph ^ 1u, c, kSiteEmpty, j, true);
-        if (ok) mbar_arrive_expect_tx(&c->full[s], kKvcBytes + kKpeBytes);
-      }
+      if (lane == 0) ok = wait(&c->empty[s], ((uint32_t)(j / kStages) & 1u) ^ 1u, c, kSiteEmpty, j);
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) return;
-      if (lane < kTK / 4) {
-        int32_t y[4];
+      if (!ok) break;
+      const uint32_t stage = sbase + kOffKvc + s * kKvcStage;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int64_t pos = (int64_t)t * kTK + lane * 4 + q;
-          y[q] = (int32_t)(pos < N ? resolve_slot(p, b, pos) : 0);
+      for (int tt = 0; tt < kTokPerWarp; ++tt) {
+        const int64_t sl = __shfl_sync(0xffffffffu, slot, tt);
+        const int r = r0 + tt;
+        const __nv_bfloat16* src = kvc_g + sl * p.kv_c_stride;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int g = lane + 32 * h;  // 16-byte piece of the row
+          const int ch = g >> 3, q = g & 7;
+          cp_async_16(stage + ch * kChunk + r * 128 + ((q ^ (r & 7)) << 4), src + g * 8);
         }
-        uint8_t* kvc = smem + kOffKvc + s * kKvcStage + lane * 512;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          tma_gather4_mc(kvc + ch * kChunk, map_kvc, ch * 64, y[0], y[1], y[2], y[3], &c->full[s], 0x3);
-        tma_gather4(smem + kOffKpe + s * kKpeBytes + lane * 512, map_kpe, 0, y[0], y[1], y[2], y[3],
-                    &c->full[s]);
       }
-      __syncwarp();
+      if (with_kpe) {
+        const uint32_t kst = sbase + kOffKpe + s * kKpeBytes;
+#pragma unroll
+        for (int gg = 0; gg < kTokPerWarp / 4; ++gg) {
+          const int tt = gg * 4 + (lane >> 3), q = lane & 7;
+          const int64_t sl = __shfl_sync(0xffffffffu, slot, tt);
+          const int r = r0 + tt;
+          cp_async_16(kst + r * 128 + ((q ^ (r & 7)) << 4), kpe_g + sl * p.k_pe_stride + q * 8);
+        }
+      }
+      cp_async_mbar_arrive(&c->full[s]);
     }
   }
-  // drain: the last stages' copies must land before this CTA may exit
-  if (lane == 0 && c->abort) {
-    for (int q = j - kStages; q < j; ++q)
-      if (q >= 0) mbar_wait_drain(&c->full[q % kStages], (uint32_t)(q / kStages) & 1u, kDrainLimitNs);
-  }
+  // copies already issued must land before this CTA may exit
+  cp_async_wait_all();
 }
 
+// ---------------------------------------------------------------------------
+// score CTA roles
+// ---------------------------------------------------------------------------
 __device__ void score_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id, int n_clusters) {
   const uint32_t tS = c->tmem_base;        // columns [0, 128): two S buffers
   const uint32_t tQ = c->tmem_base + 128;  // columns [128, 416): queries, bf16 pairs
@@ -202,19 +237,25 @@ __device__ void score_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       const int s = j % kStages, sb = j & 1;
       if (!wait(&c->full[s], (uint32_t)(j / kStages) & 1u, c, kSiteFullS, j)) return;
-      if (!wait(&c->s_free[sb], ((uint32_t)(j >> 1) & 1u) ^ 1u, c, kSiteSFree, j)) return;
+      // Issue S(j) only after the softmax has loaded S(j-1): a TMEM load waits
+      // behind MMAs issued before it, so issuing S(j) first would hold the
+      // softmax's load of S(j-1) until S(j) completes.  (This also implies
+      // buffer sb, last read for S(j-2), is free.)
+      if (j > 0 && !wait(&c->s_free[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c, kSiteSFree, j)) return;
+      fence_proxy_async_smem();  // cp.async data, written through the generic proxy, feeds the MMA
       tc_fence_after();
       // descriptors differ only in the start-address field: add (offset >> 4)
       const uint64_t dk = smem_desc(smem_u32(smem + kOffKvc + s * kKvcStage), 16, 1024, kLayoutSw128);
       const uint64_t dp = smem_desc(smem_u32(smem + kOffKpe + s * kKpeBytes), 16, 1024, kLayoutSw128);
       const uint32_t ts = tS + sb * kTK;
-#pragma unroll
+      uint64_t bd = dk;
+#pragma unroll 1
       for (int kc = 0; kc < 9; ++kc) {
+        if (kc == 8) bd = dp;  // the rope chunk lives in the k_pe stage
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bd = (kc < 8 ? dk + (uint64_t)((kc * kChunk + kk * 32) >> 4) : dp + (uint64_t)((kk * 32) >> 4));
-          mma_ts(ts, tQ + kc * 32 + kk * 8, bd, kIdescS, (kc | kk) != 0);
-        }
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(ts, tQ + kc * 32 + kk * 8, bd + (uint64_t)((kk * 32) >> 4), kIdescS, (kc | kk) != 0);
+        bd += (uint64_t)(kChunk >> 4);
       }
       mma_commit(&c->s_full[sb]);
       mma_commit(&c->empty[s]);
@@ -229,6 +270,8 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
   const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
   const uint32_t tS = c->tmem_base + lane_off;
   const uint32_t tQ = c->tmem_base + 128 + lane_off;
+  const float sl2 = p.scale_log2;
+  const int nq = p.Q;
   int j = 0, seg = 0;
   for (int64_t item = cluster_id; item < p.n_items; item += n_clusters) {
     const Item it = item_at(p, item);
@@ -237,19 +280,17 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
     const int row = it.g * kRG + r;
     const bool live = row < p.rows;
     const int64_t P = p.prefix_lens[b];
-    const int64_t N = P + p.Q;
     const uint64_t anc = live ? p.anc[(int64_t)b * p.Q + row / p.H] : 0ull;
 
     // stage this item's queries into TMEM: column c holds elements 2c, 2c+1
     {
-      __syncwarp();
       const uint4* ql = reinterpret_cast<const uint4*>(p.q_lat) + ((int64_t)b * p.rows + row) * (kDl / 8);
       const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe) + ((int64_t)b * p.rows + row) * (kDr / 8);
 #pragma unroll 1
-      for (int c0 = 0; c0 < 288; c0 += 32) {
-        uint32_t w[32];
+      for (int c0 = 0; c0 < 288; c0 += 16) {
+        uint32_t w[16];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
+        for (int v = 0; v < 4; ++v) {
           const int col = c0 + 4 * v;  // 4 columns per 16-byte vector
           uint4 x = make_uint4(0, 0, 0, 0);
           if (live) x = col < 256 ? ql[col / 4] : qp[(col - 256) / 4];
@@ -259,7 +300,7 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
           w[4 * v + 3] = x.w;
         }
         __syncwarp();
-        tmem_st_32x32b_x32(tQ + c0, w);
+        tmem_st_32x32b_x16(tQ + c0, w);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -274,40 +315,36 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
       if (!wait(&c->s_full[sb], (uint32_t)(j >> 1) & 1u, c, kSiteSFull, j)) return;
       __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the spin
       tc_fence_after();
-      float x[kTK];
-      {
-        uint32_t u[32];
-        tmem_ld_32x32b_x32(tS + sb * kTK, u);
-        tmem_wait_ld();
-#pragma unroll
-        for (int q = 0; q < 32; ++q) x[q] = __uint_as_float(u[q]);
-        tmem_ld_32x32b_x32(tS + sb * kTK + 32, u);
-        tmem_wait_ld();
-#pragma unroll
-        for (int q = 0; q < 32; ++q) x[32 + q] = __uint_as_float(u[q]);
-      }
-      tc_fence_before();
-      mbar_arrive(&c->s_free[sb]);
+      uint32_t u[kTK];
+      tmem_ld64_sync(tS + sb * kTK, u);
 
-      // scale to base-2 units and apply the prefix + tree mask
+      // scale to base-2 units and apply the prefix + tree mask.  Only tiles
+      // reaching the tree tail need the mask; there the position relative to
+      // the first tree node lies in (-64, Q + 64).  The branch is uniform
+      // across the warp (one tile, one sequence), so it sits outside the loops.
       const int64_t pos0 = (int64_t)t * kTK;
       float tmax = -INFINITY;
-      if (pos0 + kTK <= P) {
+      if (pos0 + kTK <= P) {  // the whole tile is prefix: nothing to mask
 #pragma unroll
         for (int q = 0; q < kTK; ++q) {
-          x[q] *= p.scale_log2;
-          tmax = fmaxf(tmax, x[q]);
+          const float v = __uint_as_float(u[q]) * sl2;
+          u[q] = __float_as_uint(v);
+          tmax = fmaxf(tmax, v);
         }
       } else {
+        const int rel0 = (int)(pos0 - P);
 #pragma unroll
         for (int q = 0; q < kTK; ++q) {
-          const int64_t pos = pos0 + q;
-          const int64_t node = pos - P;
-          const bool vis = pos < P || (pos < N && ((anc >> (node & 63)) & 1ull));
-          x[q] = vis ? x[q] * p.scale_log2 : -INFINITY;
-          tmax = fmaxf(tmax, x[q]);
+          const int rel = rel0 + q;  // < 0: prefix; [0, Q): tree node rel
+          const bool vis = rel < 0 || (rel < nq && ((anc >> (rel & 63)) & 1ull));
+          const float v = vis ? __uint_as_float(u[q]) * sl2 : -INFINITY;
+          u[q] = __float_as_uint(v);
+          tmax = fmaxf(tmax, v);
         }
       }
+      // every loaded value has been consumed: the next S MMA may start
+      tc_fence_before();
+      mbar_arrive(&c->s_free[sb]);
       // lazy running max: move it only when this tile beats it by > 8 (x 2^8)
       float alpha = 1.f;
       const bool need = tmax > m + 8.f;
@@ -322,34 +359,30 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
       // wait until the value CTA is done with this P buffer
       if (!wait(&c->p_free[sb], ((uint32_t)(j >> 1) & 1u) ^ 1u, c, kSitePFree, j, true)) return;
       const uint32_t pbase = mapa_shared(smem_u32(smem + kOffP + sb * kPBytes), 1);
+      const uint32_t pbar = mapa_shared(smem_u32(&c->p_full[sb]), 1);
 #pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) {
+      for (int q8 = 0; q8 < kTK / 8; ++q8) {
         float e[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          e[u] = exp2f(x[8 * q8 + u] - mu);
-          lx += e[u];
+        for (int v = 0; v < 8; ++v) {
+          e[v] = ex2_approx(__uint_as_float(u[8 * q8 + v]) - mu);
+          lx += e[v];
         }
         const uint32_t w0 = pack_bf16(e[0], e[1]), w1 = pack_bf16(e[2], e[3]);
         const uint32_t w2 = pack_bf16(e[4], e[5]), w3 = pack_bf16(e[6], e[7]);
         // the row sum uses the rounded values the value CTA multiplies by
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w0);
-        float2 f0 = __bfloat1622float2(h[0]);
-        l += f0.x + f0.y;
-        f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w1));
-        l += f0.x + f0.y;
-        f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w2));
-        l += f0.x + f0.y;
-        f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w3));
-        l += f0.x + f0.y;
-        st_cluster_v4(pbase + sw128_offset(r, 8 * q8), w0, w1, w2, w3);
+        float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w0));
+        l += f.x + f.y;
+        f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w1));
+        l += f.x + f.y;
+        f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w2));
+        l += f.x + f.y;
+        f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w3));
+        l += f.x + f.y;
+        st_async_v4(pbase + sw128_offset(r, 8 * q8), w0, w1, w2, w3, pbar);
       }
-      // every row ships its factor; rows that moved their max also raise the
-      // tile's flag (the value CTA clears it when it releases the buffer)
-      st_cluster_f32(mapa_shared(smem_u32(&c->alpha[sb][r]), 1), alpha);
-      if (need) red_or_cluster(mapa_shared(smem_u32(&c->flag[sb]), 1), 1u);
-      fence_proxy_async_cluster();
-      mbar_arrive_cluster(&c->p_full[sb], 1);
+      // every row ships its factor; the bytes themselves complete p_full
+      st_async_f32(mapa_shared(smem_u32(&c->alpha[sb][r]), 1), alpha, pbar);
     }
 
     // hand the row statistics to the value CTA for the epilogue
@@ -367,18 +400,27 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
 // ---------------------------------------------------------------------------
 __device__ void value_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id, int n_clusters) {
   const uint32_t tO = c->tmem_base;
-  int j = 0, seg = 0, ncmd = 0;
+  int j = 0, ncmd = 0;
   bool ok = true;
   for (int64_t item = cluster_id; item < p.n_items && ok; item += n_clusters) {
     const Item it = item_at(p, item);
     if (it.t1 <= it.t0) continue;
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       const int s = j % kStages, pb = j & 1;
-      mbar_arrive_expect_tx(&c->full[s], kKvcBytes);
       if (!(ok = wait(&c->full[s], (uint32_t)(j / kStages) & 1u, c, kSiteFullV, j))) break;
+      mbar_arrive_expect_tx(&c->p_full[pb], kPTxBytes);
       if (!(ok = wait(&c->p_full[pb], (uint32_t)(j >> 1) & 1u, c, kSitePFull, j, true))) break;
       const bool first = (t == it.t0);
-      if (!first && c->flag[pb]) {
+      bool rescale = false;
+      if (!first) {
+        const float4* a4 = reinterpret_cast<const float4*>(c->alpha[pb]);
+#pragma unroll 8
+        for (int i = 0; i < kRG / 4; ++i) {
+          const float4 a = a4[i];
+          rescale |= (a.x != 1.f) | (a.y != 1.f) | (a.z != 1.f) | (a.w != 1.f);
+        }
+      }
+      if (rescale) {
         // O must hold PV(j-1) in full before it is rescaled
         if (!(ok = wait(&c->pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c, kSitePvPrev, j))) break;
         tc_fence_after();
@@ -388,9 +430,10 @@ __device__ void value_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id
         if (!(ok = wait(&c->cmd_done, (uint32_t)ncmd & 1u, c, kSiteCmdDone, j))) break;
         ++ncmd;
       }
+      fence_proxy_async_smem();
       tc_fence_after();
       const uint64_t da = smem_desc(smem_u32(smem + kOffP + pb * kPBytes), 16, 1024, kLayoutSw128);
-      const uint64_t dv = smem_desc(smem_u32(smem + kOffKvc + s * kKvcStage), MLA_TC_V_LBO, MLA_TC_V_SBO,
+      const uint64_t dv = smem_desc(smem_u32(smem + kOffKvc + s * kKvcStage), kVAtomStrideN, kVGroupStrideK,
                                     kLayoutSw128);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
@@ -401,6 +444,7 @@ __device__ void value_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id
         }
       }
       mma_commit(&c->pv_done[pb]);
+      mma_commit(&c->empty[s]);
     }
     if (!ok) break;
     // epilogue of this item once its last PV is complete
@@ -411,29 +455,24 @@ __device__ void value_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id
     mbar_arrive(&c->cmd_full);
     if (!(ok = wait(&c->cmd_done, (uint32_t)ncmd & 1u, c, kSiteCmdDone, j))) break;
     ++ncmd;
-    ++seg;
   }
   c->cmd = kCmdExit;
   mbar_arrive(&c->cmd_full);
   if (c->abort) {
-    // drain: outstanding MMAs and multicast copies into this CTA
+    // outstanding PV MMAs must finish before TMEM is released
     mma_commit(&c->drain);
     mbar_wait_drain(&c->drain, 0, kDrainLimitNs);
-    for (int q = j - kStages + 1; q <= j; ++q)
-      if (q >= 0) mbar_wait_drain(&c->full[q % kStages], (uint32_t)(q / kStages) & 1u, kDrainLimitNs);
   }
 }
 
-// Releases each tile's stage and P buffer back to the score CTA once the PV
-// MMAs that read them have completed.
+// Releases each tile's P buffer back to the score CTA once the PV MMAs that
+// read it have completed.
 __device__ void value_release(const Params& p, Ctl* c, int cluster_id, int n_clusters) {
   int j = 0;
   for (int64_t item = cluster_id; item < p.n_items; item += n_clusters) {
     const Item it = item_at(p, item);
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       if (!wait(&c->pv_done[j & 1], (uint32_t)(j >> 1) & 1u, c, kSiteRelease, j)) return;
-      c->flag[j & 1] = 0;  // ordered before the release below
-      mbar_arrive_cluster(&c->empty[j % kStages], 0);
       mbar_arrive_cluster(&c->p_free[j & 1], 0);
     }
   }
@@ -458,8 +497,7 @@ __device__ void value_epilogue(const Params& p, Ctl* c) {
 #pragma unroll 1
       for (int c0 = 0; c0 < kDl; c0 += 32) {
         uint32_t u[32];
-        tmem_ld_32x32b_x32(tO + c0, u);
-        tmem_wait_ld();
+        tmem_ld32_sync(tO + c0, u);
 #pragma unroll
         for (int q = 0; q < 32; ++q) u[q] = __float_as_uint(__uint_as_float(u[q]) * a);
         tmem_st_32x32b_x32(tO + c0, u);
@@ -483,8 +521,7 @@ __device__ void value_epilogue(const Params& p, Ctl* c) {
         for (int c0 = 0; c0 < kDl; c0 += 32) {
           uint32_t u[32];
           __syncwarp();
-          tmem_ld_32x32b_x32(tO + c0, u);
-          tmem_wait_ld();
+          tmem_ld32_sync(tO + c0, u);
           if (live) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
@@ -505,8 +542,7 @@ __device__ void value_epilogue(const Params& p, Ctl* c) {
         for (int c0 = 0; c0 < kDl; c0 += 32) {
           uint32_t u[32];
           __syncwarp();
-          tmem_ld_32x32b_x32(tO + c0, u);
-          tmem_wait_ld();
+          tmem_ld32_sync(tO + c0, u);
           if (live) {
 #pragma unroll
             for (int v = 0; v < 8; ++v)
@@ -522,9 +558,7 @@ __device__ void value_epilogue(const Params& p, Ctl* c) {
   }
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const Params p, const __grid_constant__ CUtensorMap map_kvc,
-                   const __grid_constant__ CUtensorMap map_kpe) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_tc_kernel(const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
   const uint32_t rank = cluster_ctarank();
@@ -539,16 +573,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   Ctl* c = reinterpret_cast<Ctl*>(smem + kOffCtl);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&c->full[s], 1);
-      mbar_init(&c->empty[s], 2);
+      mbar_init(&c->full[s], kProducerThreads);
+      mbar_init(&c->empty[s], 1);
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(&c->s_full[q], 1);
       mbar_init(&c->s_free[q], kRG);
       mbar_init(&c->p_free[q], 1);
-      mbar_init(&c->p_full[q], kRG);
+      mbar_init(&c->p_full[q], 1);
       mbar_init(&c->pv_done[q], 1);
-      c->flag[q] = 0;
     }
     mbar_init(&c->q_ready, kRG);
     mbar_init(&c->fin_free, kRG);
@@ -560,13 +593,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     c->abort_site = 0;
     fence_mbar_init();
   }
-  if (warp == 2) {
+  if (warp == kWarpTmem) {
     tmem_alloc(&c->tmem_base, kTmemCols);
     tmem_relinquish();
-  }
-  if (threadIdx.x == 64 && rank == 0) {
-    prefetch_tmap(&map_kvc);
-    prefetch_tmap(&map_kpe);
   }
   tc_fence_before();
   cluster_sync();  // barriers of both CTAs initialised before any remote use
@@ -574,14 +603,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   const int cluster_id = blockIdx.x >> 1;
   const int n_clusters = gridDim.x >> 1;
-  if (rank == 0) {
-    if (warp == 0) score_producer(p, &map_kvc, &map_kpe, smem, c, cluster_id, n_clusters);
-    else if (warp == 1) { if ((threadIdx.x & 31) == 0) score_mma(p, smem, c, cluster_id, n_clusters); }
-    else if (warp >= 4) score_softmax(p, smem, c, cluster_id, n_clusters);
+  if (warp < kProducerWarps) {
+    producer(p, smem, c, warp, rank == 0, cluster_id, n_clusters);
+  } else if (rank == 0) {
+    if (warp == kWarpMma) { if ((threadIdx.x & 31) == 0) score_mma(p, smem, c, cluster_id, n_clusters); }
+    else if (warp >= kWarpRows) score_softmax(p, smem, c, cluster_id, n_clusters);
   } else {
-    if (warp == 1) { if ((threadIdx.x & 31) == 0) value_mma(p, smem, c, cluster_id, n_clusters); }
-    else if (warp == 2) { if ((threadIdx.x & 31) == 0) value_release(p, c, cluster_id, n_clusters); }
-    else if (warp >= 4) value_epilogue(p, c);
+    if (warp == kWarpMma) { if ((threadIdx.x & 31) == 0) value_mma(p, smem, c, cluster_id, n_clusters); }
+    else if (warp == kWarpRelease) { if ((threadIdx.x & 31) == 0) value_release(p, c, cluster_id, n_clusters); }
+    else if (warp >= kWarpRows) value_epilogue(p, c);
   }
 
   __syncwarp();
@@ -595,46 +625,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && c->abort) {
     set_err(p.err, MLA_DEVERR_TIMEOUT);
     atomicCAS(p.err + 1, 0u, (uint32_t)c->abort_site | (rank << 8));
-    // let multicast copies issued by the peer before it stopped land here
-    const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < kDrainLimitNs) {
-    }
   }
   __syncthreads();
   tc_fence_after();
   cluster_sync();  // no CTA leaves while its peer may still touch its shared memory
-  if (warp == 2) tmem_dealloc(c->tmem_base, kTmemCols);
-}
-
-// ---------------------------------------------------------------------------
-// host side
-// ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaDriverEntryPointQueryResult q;
-    void* f = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
-// Rows of a pool tensor as a 2-D map: width columns, 64-column boxes, one row
-// per box (the shape tile::gather4 expects), 128-byte swizzle.
-bool make_row_map(CUtensorMap* m, const void* base, int64_t width, int64_t stride_elems, int64_t rows) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)stride_elems * 2};
-  cuuint32_t box[2] = {64, 1};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (warp == kWarpTmem) tmem_dealloc(c->tmem_base, kTmemCols);
 }
 
 }  // namespace tc
@@ -662,14 +657,10 @@ int tc_clusters_per_gpu(int sm_count) {
 }
 
 cudaError_t launch_attn_tc(const Params& p, cudaStream_t stream) {
-  CUtensorMap map_kvc, map_kpe;
-  if (!tc::make_row_map(&map_kvc, p.kv_c, kDl, p.kv_c_stride, p.pool_slots) ||
-      !tc::make_row_map(&map_kpe, p.k_pe, kDr, p.k_pe_stride, p.pool_slots))
-    return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(tc::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        tc::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  tc::attn_tc_kernel<<<2 * p.grid, tc::kThreads, tc::kSmemAlloc, stream>>>(p, map_kvc, map_kpe);
+  tc::attn_tc_kernel<<<2 * p.grid, tc::kThreads, tc::kSmemAlloc, stream>>>(p);
   return cudaGetLastError();
 }
 
