@@ -102,8 +102,7 @@ struct alignas(16) Ctl {
   uint64_t cmd_done;        // value: command finished (128 arrivals)
   uint64_t drain;           // both: final MMA drain on abort
   float alpha[2][kRG];      // value: per-row rescale of O before PV(j) (1 = unchanged)
-  float lfin[kRG];          // value: final row sums of the bf16-rounded p (normalises out)
-  float lxfin[kRG];         // value: final row sums of the unrounded p (gives lse)
+  float lfin[kRG];          // value: final row sums of the weights
   float mfin[kRG];          // value: final running max (base-2 units)
   uint32_t tmem_base;
   int abort;
@@ -130,6 +129,13 @@ __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, Ctl* c, int
   // first site to give up in this CTA (others follow the abort flag)
   atomicCAS(&c->abort_site, 0, (site & 0xff) | ((j & 0xffff) << 16));
   return false;
+}
+
+// The same wait made by every lane of a warp; the result is warp-uniform and
+// the warp is converged on return (the MMA roles issue with elect.sync).
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, Ctl* c, int site, int j,
+                                          bool cluster = false) {
+  return __all_sync(0xffffffffu, wait(bar, parity, c, site, j, cluster));
 }
 
 // 2^x by the hardware approximation (flushes results below 2^-126 to zero,
@@ -226,41 +232,49 @@ __device__ void producer(const Params& p, uint8_t* smem, Ctl* c, int pw, bool wi
 // score CTA roles
 // ---------------------------------------------------------------------------
 __device__ void score_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id, int n_clusters) {
+  // run by the whole warp; one elected lane issues each tcgen05 op
   const uint32_t tS = c->tmem_base;        // columns [0, 128): two S buffers
   const uint32_t tQ = c->tmem_base + 128;  // columns [128, 416): queries, bf16 pairs
   int j = 0, seg = 0;
-  for (int64_t item = cluster_id; item < p.n_items; item += n_clusters) {
+  bool ok = true;
+  for (int64_t item = cluster_id; item < p.n_items && ok; item += n_clusters) {
     const Item it = item_at(p, item);
     if (it.t1 <= it.t0) continue;
-    if (!wait(&c->q_ready, (uint32_t)seg & 1u, c, kSiteQReady, j)) return;
+    if (!(ok = wait_warp(&c->q_ready, (uint32_t)seg & 1u, c, kSiteQReady, j))) break;
     tc_fence_after();
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       const int s = j % kStages, sb = j & 1;
-      if (!wait(&c->full[s], (uint32_t)(j / kStages) & 1u, c, kSiteFullS, j)) return;
+      if (!(ok = wait_warp(&c->full[s], (uint32_t)(j / kStages) & 1u, c, kSiteFullS, j))) break;
       // Issue S(j) only after the softmax has loaded S(j-1): a TMEM load waits
       // behind MMAs issued before it, so issuing S(j) first would hold the
       // softmax's load of S(j-1) until S(j) completes.  (This also implies
       // buffer sb, last read for S(j-2), is free.)
-      if (j > 0 && !wait(&c->s_free[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c, kSiteSFree, j)) return;
+      if (j > 0 && !(ok = wait_warp(&c->s_free[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c, kSiteSFree, j)))
+        break;
       fence_proxy_async_smem();  // cp.async data, written through the generic proxy, feeds the MMA
       tc_fence_after();
       // descriptors differ only in the start-address field: add (offset >> 4)
       const uint64_t dk = smem_desc(smem_u32(smem + kOffKvc + s * kKvcStage), 16, 1024, kLayoutSw128);
       const uint64_t dp = smem_desc(smem_u32(smem + kOffKpe + s * kKpeBytes), 16, 1024, kLayoutSw128);
       const uint32_t ts = tS + sb * kTK;
-      uint64_t bd = dk;
-#pragma unroll 1
+#pragma unroll
       for (int kc = 0; kc < 9; ++kc) {
-        if (kc == 8) bd = dp;  // the rope chunk lives in the k_pe stage
+        // chunks 0-7: the latent part in the kv_c stage; chunk 8: the rope part in the k_pe stage
+        const uint64_t bd = kc < 8 ? dk + (uint64_t)((kc * kChunk) >> 4) : dp;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_ts(ts, tQ + kc * 32 + kk * 8, bd + (uint64_t)((kk * 32) >> 4), kIdescS, (kc | kk) != 0);
-        bd += (uint64_t)(kChunk >> 4);
+          mma_ts_warp(ts, tQ + kc * 32 + kk * 8, bd + (uint64_t)((kk * 32) >> 4), kIdescS, (kc | kk) != 0);
       }
-      mma_commit(&c->s_full[sb]);
-      mma_commit(&c->empty[s]);
+      mma_commit_warp(&c->s_full[sb]);
+      mma_commit_warp(&c->empty[s]);
     }
     ++seg;
+  }
+  if (__any_sync(0xffffffffu, c->abort != 0)) {
+    // outstanding S MMAs must finish before TMEM is released
+    mma_commit_warp(&c->drain);
+    if ((threadIdx.x & 31) == 0) mbar_wait_drain(&c->drain, 0, kDrainLimitNs);
+    __syncwarp();
   }
 }
 
@@ -307,9 +321,9 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
       mbar_arrive(&c->q_ready);
     }
 
-    // l sums the bf16-rounded weights the value CTA multiplies by, so out is
-    // normalised consistently; lx sums the unrounded weights for an exact lse
-    float m = -INFINITY, l = 0.f, lx = 0.f;
+    // m: running max of the scaled scores (base-2 units); l: running sum of
+    // the weights 2^(score - m), accumulated in fp32 before bf16 rounding
+    float m = -INFINITY, l = 0.f;
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       const int sb = j & 1;
       if (!wait(&c->s_full[sb], (uint32_t)(j >> 1) & 1u, c, kSiteSFull, j)) return;
@@ -317,70 +331,62 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
       tc_fence_after();
       uint32_t u[kTK];
       tmem_ld64_sync(tS + sb * kTK, u);
+      // the tile is in registers: the next S MMA may overwrite this buffer
+      tc_fence_before();
+      mbar_arrive(&c->s_free[sb]);
 
-      // scale to base-2 units and apply the prefix + tree mask.  Only tiles
-      // reaching the tree tail need the mask; there the position relative to
-      // the first tree node lies in (-64, Q + 64).  The branch is uniform
-      // across the warp (one tile, one sequence), so it sits outside the loops.
+      // prefix + tree mask on the raw scores.  Only tiles reaching the tree
+      // tail need it; there the position relative to the first tree node lies
+      // in (-64, Q + 64).  The branch is uniform across the warp (one tile,
+      // one sequence), so it sits outside the loop.
       const int64_t pos0 = (int64_t)t * kTK;
-      float tmax = -INFINITY;
-      if (pos0 + kTK <= P) {  // the whole tile is prefix: nothing to mask
-#pragma unroll
-        for (int q = 0; q < kTK; ++q) {
-          const float v = __uint_as_float(u[q]) * sl2;
-          u[q] = __float_as_uint(v);
-          tmax = fmaxf(tmax, v);
-        }
-      } else {
+      if (pos0 + kTK > P) {
         const int rel0 = (int)(pos0 - P);
 #pragma unroll
         for (int q = 0; q < kTK; ++q) {
           const int rel = rel0 + q;  // < 0: prefix; [0, Q): tree node rel
           const bool vis = rel < 0 || (rel < nq && ((anc >> (rel & 63)) & 1ull));
-          const float v = vis ? __uint_as_float(u[q]) * sl2 : -INFINITY;
-          u[q] = __float_as_uint(v);
-          tmax = fmaxf(tmax, v);
+          if (!vis) u[q] = 0xff800000u;  // -inf
         }
       }
-      // every loaded value has been consumed: the next S MMA may start
-      tc_fence_before();
-      mbar_arrive(&c->s_free[sb]);
+      // row max of the raw scores in eight independent chains; the scale is
+      // positive, so scaling the max equals the max of the scaled scores
+      float mx[8];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) mx[v] = __uint_as_float(u[v]);
+#pragma unroll
+      for (int q = 8; q < kTK; ++q) mx[q & 7] = fmaxf(mx[q & 7], __uint_as_float(u[q]));
+      const float tmax =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+          sl2;
       // lazy running max: move it only when this tile beats it by > 8 (x 2^8)
       float alpha = 1.f;
-      const bool need = tmax > m + 8.f;
-      if (need) {
+      if (tmax > m + 8.f) {
         alpha = exp2f(m - tmax);  // 0 when m is -inf
         l *= alpha;
-        lx *= alpha;
         m = tmax;
       }
-      const float mu = (m == -INFINITY) ? 0.f : m;
+      const float nmu = (m == -INFINITY) ? 0.f : -m;
 
       // wait until the value CTA is done with this P buffer
       if (!wait(&c->p_free[sb], ((uint32_t)(j >> 1) & 1u) ^ 1u, c, kSitePFree, j, true)) return;
       const uint32_t pbase = mapa_shared(smem_u32(smem + kOffP + sb * kPBytes), 1);
       const uint32_t pbar = mapa_shared(smem_u32(&c->p_full[sb]), 1);
+      // weights 2^(s * scale - m) as bf16, shipped 16 bytes at a time
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int q8 = 0; q8 < kTK / 8; ++q8) {
-        float e[8];
+        uint32_t w[4];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          e[v] = ex2_approx(__uint_as_float(u[8 * q8 + v]) - mu);
-          lx += e[v];
+        for (int v = 0; v < 4; ++v) {
+          const float e0 = ex2_approx(fmaf(__uint_as_float(u[8 * q8 + 2 * v]), sl2, nmu));
+          const float e1 = ex2_approx(fmaf(__uint_as_float(u[8 * q8 + 2 * v + 1]), sl2, nmu));
+          ls[v] += e0 + e1;
+          w[v] = pack_bf16(e0, e1);
         }
-        const uint32_t w0 = pack_bf16(e[0], e[1]), w1 = pack_bf16(e[2], e[3]);
-        const uint32_t w2 = pack_bf16(e[4], e[5]), w3 = pack_bf16(e[6], e[7]);
-        // the row sum uses the rounded values the value CTA multiplies by
-        float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w0));
-        l += f.x + f.y;
-        f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w1));
-        l += f.x + f.y;
-        f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w2));
-        l += f.x + f.y;
-        f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w3));
-        l += f.x + f.y;
-        st_async_v4(pbase + sw128_offset(r, 8 * q8), w0, w1, w2, w3, pbar);
+        st_async_v4(pbase + sw128_offset(r, 8 * q8), w[0], w[1], w[2], w[3], pbar);
       }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       // every row ships its factor; the bytes themselves complete p_full
       st_async_f32(mapa_shared(smem_u32(&c->alpha[sb][r]), 1), alpha, pbar);
     }
@@ -388,7 +394,6 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
     // hand the row statistics to the value CTA for the epilogue
     if (!wait(&c->fin_free, ((uint32_t)seg & 1u) ^ 1u, c, kSiteFinFree, j, true)) return;
     st_cluster_f32(mapa_shared(smem_u32(&c->lfin[r]), 1), l);
-    st_cluster_f32(mapa_shared(smem_u32(&c->lxfin[r]), 1), lx);
     st_cluster_f32(mapa_shared(smem_u32(&c->mfin[r]), 1), m);
     mbar_arrive_cluster(&c->fin_full, 1);
     ++seg;
@@ -399,7 +404,10 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
 // value CTA roles
 // ---------------------------------------------------------------------------
 __device__ void value_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id, int n_clusters) {
+  // run by the whole warp; one elected lane issues each tcgen05 op, lane 0
+  // makes the single-count arrivals
   const uint32_t tO = c->tmem_base;
+  const int lane = threadIdx.x & 31;
   int j = 0, ncmd = 0;
   bool ok = true;
   for (int64_t item = cluster_id; item < p.n_items && ok; item += n_clusters) {
@@ -407,27 +415,25 @@ __device__ void value_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id
     if (it.t1 <= it.t0) continue;
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       const int s = j % kStages, pb = j & 1;
-      if (!(ok = wait(&c->full[s], (uint32_t)(j / kStages) & 1u, c, kSiteFullV, j))) break;
-      mbar_arrive_expect_tx(&c->p_full[pb], kPTxBytes);
-      if (!(ok = wait(&c->p_full[pb], (uint32_t)(j >> 1) & 1u, c, kSitePFull, j, true))) break;
+      if (!(ok = wait_warp(&c->full[s], (uint32_t)(j / kStages) & 1u, c, kSiteFullV, j))) break;
+      if (lane == 0) mbar_arrive_expect_tx(&c->p_full[pb], kPTxBytes);
+      if (!(ok = wait_warp(&c->p_full[pb], (uint32_t)(j >> 1) & 1u, c, kSitePFull, j, true))) break;
       const bool first = (t == it.t0);
       bool rescale = false;
       if (!first) {
-        const float4* a4 = reinterpret_cast<const float4*>(c->alpha[pb]);
-#pragma unroll 8
-        for (int i = 0; i < kRG / 4; ++i) {
-          const float4 a = a4[i];
-          rescale |= (a.x != 1.f) | (a.y != 1.f) | (a.z != 1.f) | (a.w != 1.f);
-        }
+        const float4 a = reinterpret_cast<const float4*>(c->alpha[pb])[lane];  // 4 of the 128 rows per lane
+        rescale = __any_sync(0xffffffffu, (a.x != 1.f) | (a.y != 1.f) | (a.z != 1.f) | (a.w != 1.f));
       }
       if (rescale) {
         // O must hold PV(j-1) in full before it is rescaled
-        if (!(ok = wait(&c->pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c, kSitePvPrev, j))) break;
+        if (!(ok = wait_warp(&c->pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c, kSitePvPrev, j))) break;
         tc_fence_after();
-        c->cmd = kCmdRescale;
-        c->cmd_buf = pb;
-        mbar_arrive(&c->cmd_full);
-        if (!(ok = wait(&c->cmd_done, (uint32_t)ncmd & 1u, c, kSiteCmdDone, j))) break;
+        if (lane == 0) {
+          c->cmd = kCmdRescale;
+          c->cmd_buf = pb;
+          mbar_arrive(&c->cmd_full);
+        }
+        if (!(ok = wait_warp(&c->cmd_done, (uint32_t)ncmd & 1u, c, kSiteCmdDone, j))) break;
         ++ncmd;
       }
       fence_proxy_async_smem();
@@ -439,30 +445,35 @@ __device__ void value_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id
       for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
         for (int nh = 0; nh < 2; ++nh) {
-          mma_ss(tO + nh * 256, da + (uint64_t)((kk * 32) >> 4),
-                 dv + (uint64_t)((nh * 4 * kChunk + kk * 16 * 128) >> 4), kIdescPV, !(first && kk == 0));
+          mma_ss_warp(tO + nh * 256, da + (uint64_t)((kk * 32) >> 4),
+                      dv + (uint64_t)((nh * 4 * kChunk + kk * 16 * 128) >> 4), kIdescPV, !(first && kk == 0));
         }
       }
-      mma_commit(&c->pv_done[pb]);
-      mma_commit(&c->empty[s]);
+      mma_commit_warp(&c->pv_done[pb]);
+      mma_commit_warp(&c->empty[s]);
     }
     if (!ok) break;
     // epilogue of this item once its last PV is complete
-    if (!(ok = wait(&c->pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c, kSitePvLast, j))) break;
+    if (!(ok = wait_warp(&c->pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c, kSitePvLast, j))) break;
     tc_fence_after();
-    c->cmd = kCmdEpilogue;
-    c->cmd_item = item;
-    mbar_arrive(&c->cmd_full);
-    if (!(ok = wait(&c->cmd_done, (uint32_t)ncmd & 1u, c, kSiteCmdDone, j))) break;
+    if (lane == 0) {
+      c->cmd = kCmdEpilogue;
+      c->cmd_item = item;
+      mbar_arrive(&c->cmd_full);
+    }
+    if (!(ok = wait_warp(&c->cmd_done, (uint32_t)ncmd & 1u, c, kSiteCmdDone, j))) break;
     ++ncmd;
   }
-  c->cmd = kCmdExit;
-  mbar_arrive(&c->cmd_full);
-  if (c->abort) {
-    // outstanding PV MMAs must finish before TMEM is released
-    mma_commit(&c->drain);
-    mbar_wait_drain(&c->drain, 0, kDrainLimitNs);
+  if (lane == 0) {
+    c->cmd = kCmdExit;
+    mbar_arrive(&c->cmd_full);
   }
+  if (__any_sync(0xffffffffu, c->abort != 0)) {
+    // outstanding PV MMAs must finish before TMEM is released
+    mma_commit_warp(&c->drain);
+    if (lane == 0) mbar_wait_drain(&c->drain, 0, kDrainLimitNs);
+  }
+  __syncwarp();
 }
 
 // Releases each tile's P buffer back to the score CTA once the PV MMAs that
@@ -507,13 +518,13 @@ __device__ void value_epilogue(const Params& p, Ctl* c) {
       const Item it = item_at(p, c->cmd_item);
       if (!wait(&c->fin_full, (uint32_t)seg & 1u, c, kSiteFinFull, seg, true)) return;
       __syncwarp();
-      const float l = c->lfin[r], lx = c->lxfin[r], m = c->mfin[r];
+      const float l = c->lfin[r], m = c->mfin[r];
       mbar_arrive_cluster(&c->fin_free, 0);
       ++seg;
       const int row = it.g * kRG + r;
       const bool live = row < p.rows;  // TMEM loads stay warp-wide; only stores are per row
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const float lse = lx > 0.f ? (m + log2f(lx)) * ln2 : -INFINITY;
+      const float lse = l > 0.f ? (m + log2f(l)) * ln2 : -INFINITY;
       const int64_t orow = (int64_t)it.b * p.rows + row;
       if (p.splits == 1) {
         uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDl);
@@ -606,10 +617,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_tc
   if (warp < kProducerWarps) {
     producer(p, smem, c, warp, rank == 0, cluster_id, n_clusters);
   } else if (rank == 0) {
-    if (warp == kWarpMma) { if ((threadIdx.x & 31) == 0) score_mma(p, smem, c, cluster_id, n_clusters); }
+    if (warp == kWarpMma) score_mma(p, smem, c, cluster_id, n_clusters);
     else if (warp >= kWarpRows) score_softmax(p, smem, c, cluster_id, n_clusters);
   } else {
-    if (warp == kWarpMma) { if ((threadIdx.x & 31) == 0) value_mma(p, smem, c, cluster_id, n_clusters); }
+    if (warp == kWarpMma) value_mma(p, smem, c, cluster_id, n_clusters);
     else if (warp == kWarpRelease) { if ((threadIdx.x & 31) == 0) value_release(p, c, cluster_id, n_clusters); }
     else if (warp >= kWarpRows) value_epilogue(p, c);
   }
@@ -617,11 +628,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_tc
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (rank == 0 && threadIdx.x == 0 && c->abort) {
-    // outstanding S MMAs must finish before TMEM is released
-    mma_commit(&c->drain);
-    mbar_wait_drain(&c->drain, 0, kDrainLimitNs);
-  }
   if (threadIdx.x == 0 && c->abort) {
     set_err(p.err, MLA_DEVERR_TIMEOUT);
     atomicCAS(p.err + 1, 0u, (uint32_t)c->abort_site | (rank << 8));
