@@ -1,49 +1,60 @@
-// Tensor-core split-KV verify attention for sm_103a: tcgen05 MMAs with TMEM
-// accumulators, asynchronous gathers of the paged KV, a 2-CTA cluster per work
-// item.
+// Tensor-core split-KV verify attention for sm_103a: tcgen05 MMAs issued for
+// CTA pairs (cta_group::2) with TMEM accumulators, asynchronous gathers of the
+// paged KV, a 4-CTA cluster per work item.
 //
-// Shape of the problem.  Per work item, 128 query rows (absorbed queries of
+// Shape of the problem.  Per work item, 256 query rows (absorbed queries of
 // (node, head) pairs; "Ground Truth in Silicon ...", section "Input Knowledge
 // Required ...", item 2) attend over KV tiles of 64 tokens whose latent kv_c
 // (512) and rope key k_pe (64) are shared by all rows ("Ground Truth in
 // Silicon ...", section "The Message in Full").  Both products are dense
-// contractions:  S = Q [128 x 576] . K^T [576 x 64]  and
-// O += P [128 x 64] . V [64 x 512]  with V = kv_c.
+// contractions:  S = Q [256 x 576] . K^T [576 x 64]  and
+// O += P [256 x 64] . V [64 x 512]  with V = kv_c.
 //
-// Why two CTAs.  An fp32 accumulator for 128 rows x 512 columns is exactly
+// Why four CTAs.  An fp32 accumulator for 128 rows x 512 columns is exactly
 // the 512 columns x 128 lanes of one SM's Tensor Memory, so O and S cannot
-// share one SM.  Each work item therefore runs on a cluster of two CTAs:
-//   * the score CTA (rank 0) keeps the 128 query rows in TMEM (288 columns,
-//     bf16 pairs) as the A operand of S = Q.K^T (TS form, M=128, N=64,
-//     K=576 in 36 steps), double-buffers S in TMEM, and runs the online
-//     softmax: one thread per row, base-2 exponent, the tree mask, and a
-//     lazy running max (the max only moves when a tile beats it by more than
+// share one SM; and the rate at which an SM can gather scattered pool rows,
+// not the tensor cores, bounds this work, so every gathered byte should feed
+// as many rows as possible.  A work item therefore runs on two CTA pairs:
+//   * the score pair (cluster ranks 0, 1) holds the 256 query rows in TMEM,
+//     128 per CTA (288 columns, bf16 pairs), as the A operand of
+//     S = Q.K^T -- one M=256 MMA for both CTAs (TS form, N=64, K=576 in 36
+//     steps), each CTA staging half of the tile's tokens (B is split along
+//     N) -- double-buffers S in TMEM, and runs the online softmax of its
+//     rows: one thread per row, base-2 exponent, the tree mask, and a lazy
+//     running max (the max only moves when a tile beats it by more than
 //     2^8, so rescaling O is rare);
-//   * the value CTA (rank 1) keeps O (512 columns) in TMEM and runs
-//     O += P.V (SS form, M=128, N=256 twice, K=64), with V read straight out
-//     of the staged kv_c tile as an MN-major operand.
-// P (bf16) and the per-row rescale factors travel from the score CTA's
-// registers into the value CTA's shared memory as st.async stores whose bytes
-// complete the value CTA's barrier.  The value CTA also writes the outputs.
+//   * the value pair (ranks 2, 3) holds O for its 128 rows per CTA (512
+//     columns) and runs O += P.V as M=256 MMAs (SS form, N=256 twice,
+//     K=64), each CTA staging half of every kv_c row (V split along N) as
+//     an MN-major operand.
+// So each staged byte serves 256 rows, half the gather of a single-CTA
+// design per row, and the smaller stages leave room for six in flight.
+// P (bf16) and the per-row rescale factors of score CTA c travel from its
+// registers into value CTA 2 + c as st.async stores whose bytes complete that
+// CTA's barrier.  The value CTAs rescale their own O rows when a factor
+// differs from 1 and write the outputs.
 //
-// Data movement.  Each CTA stages its own 64-token KV tiles, three in flight:
-// eight producer warps gather every token's pool row (kv_c, and k_pe in the
-// score CTA) with 16-byte cp.async copies written straight into the 128-byte
-// swizzled K-major layout the MMAs read, one 1 KB kv_c row per warp
-// instruction pair so each instruction reads 512 contiguous bytes; slot
-// indices are fetched one tile ahead.  Measured on GB300, the rate at which
-// one SM can gather scattered rows grows with the number of warps issuing
-// copies (outstanding requests per warp are limited): about 9 B/clk with two
-// warps and 50 B/clk with eight when the rows sit in L2; a TMA tile::gather4
-// version (four 128-byte rows per instruction) managed about 7 B/clk.  L2
-// bandwidth is ample, so each CTA loading its own copy costs nothing that
-// matters.  Each staged tile is reused by all 128 rows of the item -- the
-// head-tile reuse of "The Critical Glue: Validating a Custom Flash Attention
-// Kernel Through Test Infrastructure", section "What Came Before", widened to
-// every (node, head) row.
+// Data movement.  Eight producer warps per CTA gather the CTA's share of every
+// tile with 16-byte cp.async copies written straight into the 128-byte
+// swizzled layout the MMAs read; slot indices are fetched one tile ahead.
+// cp.async completion can only signal a barrier of the issuing CTA, so a warp
+// of each odd CTA relays "tile landed" to its pair's MMA-issuing CTA.  Each
+// staged tile is reused by all 256 rows of the item -- the head-tile reuse of
+// "The Critical Glue: Validating a Custom Flash Attention Kernel Through Test
+// Infrastructure", section "What Came Before", widened to every (node, head)
+// row.
 //
-// Every wait is bounded; on timeout the kernel sets MLA_DEVERR_TIMEOUT, stops
-// issuing work, drains what it issued, frees TMEM and returns.
+// Signals between CTAs that hand over no data of the signalling thread (a
+// buffer may be reused, a tile has landed, O is ready) use relaxed remote
+// arrives: the data they guard has already been written and observed (cp.async
+// and st.async completion, tcgen05 wait::ld / wait::st) when they are sent,
+// and a cluster-scope release arrive measured about a microsecond while the
+// thread's earlier remote stores drained.  Only the row statistics handed to
+// the value CTA (st.shared::cluster data) travel under a release arrive.
+//
+// Every wait is bounded; on timeout the kernel raises an abort flag in all
+// four CTAs, sets MLA_DEVERR_TIMEOUT, stops issuing work, drains the MMAs it
+// issued, frees TMEM and returns.
 #include "common.cuh"
 #include "sm100.cuh"
 
@@ -52,90 +63,95 @@ using namespace sm100;
 
 namespace tc {
 
-constexpr int kRG = 128;        // query rows per work item (MMA M)
-constexpr int kTK = 64;         // tokens per KV tile
-constexpr int kStages = 3;      // KV tiles in flight
+constexpr int kRG = 256;        // query rows per work item (pair MMA M)
+constexpr int kRC = 128;        // query rows per CTA
+constexpr int kTK = 64;         // tokens per KV tile (S MMA N)
+constexpr int kStages = 6;      // KV tiles in flight
 constexpr int kThreads = 512;   // 16 warps
+constexpr int kClusterCtas = 4;
 constexpr uint32_t kTmemCols = 512;
 
 // warp roles
-constexpr int kProducerWarps = 8;                  // warps 0-7
+constexpr int kProducerWarps = 8;  // warps 0-7
 constexpr int kProducerThreads = 32 * kProducerWarps;
-constexpr int kTokPerWarp = kTK / kProducerWarps;  // 8 tokens of each tile per producer warp
-constexpr int kWarpMma = 8, kWarpRelease = 9, kWarpTmem = 10, kWarpRows = 12;  // rows: 12-15
+constexpr int kWarpMma = 8;        // MMA issue (even CTAs) or tile-landed relay (odd CTAs)
+constexpr int kWarpRelease = 9;    // value: P release; score rank 1: s_free relay
+constexpr int kWarpTmem = 10, kWarpRows = 12;  // rows: 12-15
 
-constexpr int kChunk = kTK * 128;            // one 64-column bf16 chunk of a tile: 8 KB
-constexpr int kKvcStage = 8 * kChunk;        // kv_c of one tile: 64 KB
-constexpr int kOffKvc = 0;                   // [kStages][64 KB]
-constexpr int kOffKpe = kStages * kKvcStage; // score CTA: [kStages][8 KB]
-constexpr int kOffP = kStages * kKvcStage;   // value CTA: [2][16 KB]
-constexpr int kPBytes = kRG * 128;           // P tile [128 rows x 64 tokens] bf16
-constexpr int kOffCtl = kStages * kKvcStage + 2 * kPBytes;
-constexpr uint32_t kKpeBytes = kTK * kDr * 2;      // 8192
-constexpr uint32_t kPTxBytes = kPBytes + kRG * 4;  // P tile + alpha, per tile
+// score CTA stage: its 32 tokens x 576 columns, as 9 chunks of 64 columns
+// (chunks 0-7 kv_c, chunk 8 k_pe), each chunk 32 rows of 128 bytes
+constexpr int kTokS = kTK / 2;
+constexpr int kTokSPerWarp = kTokS / kProducerWarps;  // 4
+constexpr int kChunkS = kTokS * 128;                  // 4 KB
+constexpr int kStageS = 9 * kChunkS;                  // 36 KB
+// value CTA stage: 64 tokens x its 256 kv_c columns, as 4 atoms of 64 columns
+// (atom a covers columns 256 (a >> 1) + 128 half + 64 (a & 1) + [0, 64))
+constexpr int kTokVPerWarp = kTK / kProducerWarps;  // 8
+constexpr int kAtomV = kTK * 128;                   // 8 KB
+constexpr int kStageV = 4 * kAtomV;                 // 32 KB
+constexpr int kOffP = kStages * kStageV;            // value CTA: [2][16 KB]
+constexpr int kPBytes = kRC * 128;                  // P tile [128 rows x 64 tokens] bf16
+constexpr int kOffCtl = kOffP + 2 * kPBytes;
+constexpr uint32_t kPTxBytes = kPBytes + kRC * 4;   // P tile + alpha, per tile
 
-// Byte strides of the MN-major V operand (tile chunk = 64 columns x 64 rows):
-// between 64-column atoms along N, and between 8-row groups along K.
-constexpr uint32_t kVAtomStrideN = kChunk;   // 8192
-constexpr uint32_t kVGroupStrideK = 1024;
-
-constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTK, 0, 0);   // A (Q, TMEM), B (K tile) K-major
-constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);  // A (P) K-major, B (V) MN-major
+constexpr uint32_t kIdescS = idesc_bf16_f32(kRG, kTK, 0, 0);  // A (Q, TMEM), B (K tile) K-major
+constexpr uint32_t kIdescPV = idesc_bf16_f32(kRG, 256, 0, 1); // A (P) K-major, B (V) MN-major
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 20000000ull;   // 20 ms per drain wait on abort
 
-enum { kCmdRescale = 1, kCmdEpilogue = 2, kCmdExit = 3 };
-
 struct alignas(16) Ctl {
-  uint64_t full[kStages];   // KV tile landed (kProducerThreads cp.async arrivals)
-  uint64_t empty[kStages];  // stage reusable: the MMAs reading it are complete
-  uint64_t s_full[2];       // score: S tile in TMEM
-  uint64_t s_free[2];       // score: softmax has read S (128 arrivals)
-  uint64_t p_free[2];       // score: value CTA finished with its P buffer
-  uint64_t q_ready;         // score: queries staged in TMEM (128 arrivals)
-  uint64_t fin_free;        // score: value CTA consumed lfin/mfin (128 remote arrivals)
-  uint64_t p_full[2];       // value: P tile and alpha landed (st.async bytes; armed by the MMA thread)
-  uint64_t pv_done[2];      // value: PV MMAs of a tile complete
-  uint64_t fin_full;        // value: lfin/mfin written (128 remote arrivals)
-  uint64_t cmd_full;        // value: a command for the epilogue warps
-  uint64_t cmd_done;        // value: command finished (128 arrivals)
-  uint64_t drain;           // both: final MMA drain on abort
-  float alpha[2][kRG];      // value: per-row rescale of O before PV(j) (1 = unchanged)
-  float lfin[kRG];          // value: final row sums of the weights
-  float mfin[kRG];          // value: final running max (base-2 units)
+  uint64_t full[kStages];       // this CTA's share of a tile landed (kProducerThreads cp.async arrivals)
+  uint64_t full_peer[kStages];  // even CTAs: the odd CTA's share landed (1 relayed arrival)
+  uint64_t empty[kStages];      // stage reusable: the pair MMAs reading it are complete
+  uint64_t s_full[2];           // score: S tile in TMEM
+  uint64_t s_free[2];           // score: this CTA's softmax warps loaded S (4 warp arrivals; rank 0: +1 relayed)
+  uint64_t q_ready;             // score, rank 0: both CTAs' queries in TMEM (8 warp arrivals)
+  uint64_t p_free[2];           // score: the value partner finished with its P buffer
+  uint64_t fin_free;            // score: the value partner consumed lfin/mfin (128 arrivals)
+  uint64_t p_full[2];           // value: P tile and alpha landed (st.async bytes; armed by a row thread)
+  uint64_t pv_done[2];          // value: PV MMAs of a tile complete
+  uint64_t o_ready[2];          // value, rank 2: both CTAs' O ready for the tile's PV (8 warp arrivals)
+  uint64_t fin_full;            // value: lfin/mfin written (128 remote arrivals)
+  uint64_t drain;               // even CTAs: final MMA drain on abort
+  float alpha[2][kRC];          // value: per-row rescale of O before PV(j) (1 = unchanged)
+  float lfin[kRC];              // value: final row sums of the weights
+  float mfin[kRC];              // value: final running max (base-2 units)
   uint32_t tmem_base;
   int abort;
   int abort_site;
-  int cmd;
-  int cmd_buf;
-  long long cmd_item;
 };
 constexpr int kSmemBytes = kOffCtl + (int)sizeof(Ctl);
 constexpr int kSmemAlloc = 232448;  // the per-CTA maximum; the base must be 1024-aligned
 static_assert(kSmemBytes <= kSmemAlloc, "shared memory budget");
-static_assert(kOffKpe + kStages * (int)kKpeBytes <= kOffCtl, "k_pe stages overlap control block");
+static_assert(kStages * kStageS <= kOffCtl, "score stages overlap the control block");
 static_assert(kWarpRows % 4 == 0, "the row warps must form a warpgroup (TMEM lane quadrants)");
 
 // Wait sites, recorded in the workspace's second error word when a wait gives up.
 enum {
   kSiteEmpty = 1, kSiteQReady, kSiteFullS, kSiteSFree, kSiteSFull, kSitePFree, kSiteFinFree,
-  kSiteFullV, kSitePFull, kSitePvPrev, kSiteCmdDone, kSitePvLast, kSiteRelease, kSiteCmdFull, kSiteFinFull
+  kSiteFullV, kSiteOReady, kSitePFull, kSitePvPrev, kSitePvLast, kSiteRelease, kSiteRelay, kSiteFinFull,
+  kSitePeer, kSiteSFreeRelay
 };
 
-__device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, Ctl* c, int site, int j,
-                                     bool cluster = false) {
-  if (mbar_wait(bar, parity, &c->abort, kWaitLimitNs, cluster)) return true;
-  // first site to give up in this CTA (others follow the abort flag)
+// Bounded wait on a barrier of this CTA.  Barriers that other CTAs (or pair
+// MMA commits) arrive on are waited with cluster-scope acquire.  On giving
+// up, the first site is recorded and every CTA of the cluster is told to stop.
+__device__ __noinline__ void raise_abort(Ctl* c, int site, int j) {
   atomicCAS(&c->abort_site, 0, (site & 0xff) | ((j & 0xffff) << 16));
+  for (uint32_t rk = 0; rk < kClusterCtas; ++rk) st_cluster_u32(mapa_shared(smem_u32(&c->abort), rk), 1u);
+}
+__device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, Ctl* c, int site, int j,
+                                     bool cluster = true) {
+  if (mbar_wait(bar, parity, &c->abort, kWaitLimitNs, cluster)) return true;
+  raise_abort(c, site, j);
   return false;
 }
 
 // The same wait made by every lane of a warp; the result is warp-uniform and
 // the warp is converged on return (the MMA roles issue with elect.sync).
-__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, Ctl* c, int site, int j,
-                                          bool cluster = false) {
-  return __all_sync(0xffffffffu, wait(bar, parity, c, site, j, cluster));
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, Ctl* c, int site, int j) {
+  return __all_sync(0xffffffffu, wait(bar, parity, c, site, j));
 }
 
 // 2^x by the hardware approximation (flushes results below 2^-126 to zero,
@@ -151,34 +167,49 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// ---------------------------------------------------------------------------
-// producers (both CTAs)
-// ---------------------------------------------------------------------------
-// Stages the KV tiles of this CTA's items.  Producer warp pw copies tokens
-// [8 pw, 8 pw + 8) of each tile: for every token, two warp instructions move
-// its 1 KB kv_c row (lane l moves bytes 16l.. of each half), placing 16-byte
-// piece q of 64-column chunk ch of token row r at
-//   ch * kChunk + r * 128 + ((q ^ (r & 7)) * 16)
-// -- the 128-byte swizzle of the K-major operand layout.  In the score CTA two
-// more instructions move the 128-byte k_pe rows (four tokens each).  Positions
-// past the sequence read slot 0; the softmax gives them zero weight.
-__device__ void producer(const Params& p, uint8_t* smem, Ctl* c, int pw, bool with_kpe, int cluster_id,
-                         int n_clusters) {
-  const int lane = threadIdx.x & 31;
-  const __nv_bfloat16* kvc_g = reinterpret_cast<const __nv_bfloat16*>(p.kv_c);
-  const __nv_bfloat16* kpe_g = reinterpret_cast<const __nv_bfloat16*>(p.k_pe);
-  const uint32_t sbase = smem_u32(smem);
-  const int r0 = kTokPerWarp * pw;
-  int j = 0;
+// Calls f(item, it) for the non-empty items of this cluster, in order.
+template <class F>
+__device__ __forceinline__ void for_items(const Params& p, int cluster_id, int n_clusters, F&& f) {
   for (int64_t item = cluster_id; item < p.n_items; item += n_clusters) {
     const Item it = item_at(p, item);
     if (it.t1 <= it.t0) continue;
+    if (!f(item, it)) return;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// producers (all four CTAs)
+// ---------------------------------------------------------------------------
+// Stages this CTA's share of the KV tiles of its items, placing 16-byte piece
+// q of a 128-byte row segment of token row r at  base + r * 128 + ((q ^ (r & 7)) * 16)
+// -- the 128-byte swizzle of the operand layouts.
+//   score CTA `half`: tokens [32 half, 32 half + 32) of each tile; warp pw
+//     copies 4 of them: per token two instructions move the 1 KB kv_c row
+//     (lane l moves pieces l and l + 32; chunk = piece / 8), and one more
+//     instruction moves the four 128-byte k_pe rows into chunk 8;
+//   value CTA `half`: all 64 tokens, kv_c columns [256 nh + 128 half, +128)
+//     for nh = 0, 1; warp pw copies 8 tokens, one instruction per token (lane
+//     l moves piece l & 15 of segment nh = l >> 4).
+// Positions past the sequence read slot 0; the softmax gives them zero weight.
+__device__ void producer(const Params& p, uint8_t* smem, Ctl* c, int pw, uint32_t rank, int cluster_id,
+                         int n_clusters) {
+  const int lane = threadIdx.x & 31;
+  const bool score = rank < 2;
+  const int half = (int)(rank & 1);
+  const int ntok = score ? kTokSPerWarp : kTokVPerWarp;
+  const int r0 = ntok * pw;                  // first token row of this warp within the CTA's share
+  const int tok0 = score ? half * kTokS : 0;  // the share's first token within the tile
+  const __nv_bfloat16* kvc_g = reinterpret_cast<const __nv_bfloat16*>(p.kv_c);
+  const __nv_bfloat16* kpe_g = reinterpret_cast<const __nv_bfloat16*>(p.k_pe);
+  const uint32_t sbase = smem_u32(smem);
+  int j = 0;
+  for_items(p, cluster_id, n_clusters, [&](int64_t, const Item& it) {
     const int b = it.b;
     const int64_t N = (int64_t)p.prefix_lens[b] + p.Q;
     const int64_t idx0 = p.page_size == 1 ? (int64_t)p.kv_indptr[b] : 0;
-    // slot of token r0 + (lane % 8) of tile t
+    // slot of token row r0 + (lane % ntok) of tile t
     auto slot_of = [&](int t) -> int64_t {
-      const int64_t pos = (int64_t)t * kTK + r0 + (lane & (kTokPerWarp - 1));
+      const int64_t pos = (int64_t)t * kTK + tok0 + r0 + (lane & (ntok - 1));
       if (pos >= N) return 0;
       int64_t sl;
       if (p.page_size == 1) {
@@ -196,102 +227,136 @@ __device__ void producer(const Params& p, uint8_t* smem, Ctl* c, int pw, bool wi
       if (t + 1 < it.t1) next = slot_of(t + 1);  // index load for the next tile, in flight meanwhile
       bool ok = true;
       if (lane == 0) ok = wait(&c->empty[s], ((uint32_t)(j / kStages) & 1u) ^ 1u, c, kSiteEmpty, j);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      const uint32_t stage = sbase + kOffKvc + s * kKvcStage;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+      if (score) {
+        const uint32_t stage = sbase + s * kStageS;
 #pragma unroll
-      for (int tt = 0; tt < kTokPerWarp; ++tt) {
-        const int64_t sl = __shfl_sync(0xffffffffu, slot, tt);
-        const int r = r0 + tt;
-        const __nv_bfloat16* src = kvc_g + sl * p.kv_c_stride;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int g = lane + 32 * h;  // 16-byte piece of the row
-          const int ch = g >> 3, q = g & 7;
-          cp_async_16(stage + ch * kChunk + r * 128 + ((q ^ (r & 7)) << 4), src + g * 8);
-        }
-      }
-      if (with_kpe) {
-        const uint32_t kst = sbase + kOffKpe + s * kKpeBytes;
-#pragma unroll
-        for (int gg = 0; gg < kTokPerWarp / 4; ++gg) {
-          const int tt = gg * 4 + (lane >> 3), q = lane & 7;
+        for (int tt = 0; tt < kTokSPerWarp; ++tt) {
           const int64_t sl = __shfl_sync(0xffffffffu, slot, tt);
           const int r = r0 + tt;
-          cp_async_16(kst + r * 128 + ((q ^ (r & 7)) << 4), kpe_g + sl * p.k_pe_stride + q * 8);
+          const __nv_bfloat16* src = kvc_g + sl * p.kv_c_stride;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int g = lane + 32 * h;
+            const int q = g & 7;
+            cp_async_16(stage + (g >> 3) * kChunkS + r * 128 + ((q ^ (r & 7)) << 4), src + g * 8);
+          }
+        }
+        const int tt = lane >> 3, q = lane & 7;
+        const int64_t sl = __shfl_sync(0xffffffffu, slot, tt);
+        const int r = r0 + tt;
+        cp_async_16(stage + 8 * kChunkS + r * 128 + ((q ^ (r & 7)) << 4), kpe_g + sl * p.k_pe_stride + q * 8);
+      } else {
+        const uint32_t stage = sbase + s * kStageV;
+        const int nh = lane >> 4, g = lane & 15, q = g & 7;
+        const uint32_t dst0 = stage + (nh * 2 + (g >> 3)) * kAtomV;
+        const int col = nh * 256 + half * 128 + g * 8;
+#pragma unroll
+        for (int tt = 0; tt < kTokVPerWarp; ++tt) {
+          const int64_t sl = __shfl_sync(0xffffffffu, slot, tt);
+          const int r = r0 + tt;
+          cp_async_16(dst0 + r * 128 + ((q ^ (r & 7)) << 4), kvc_g + sl * p.kv_c_stride + col);
         }
       }
       cp_async_mbar_arrive(&c->full[s]);
     }
-  }
+    return true;
+  });
   // copies already issued must land before this CTA may exit
   cp_async_wait_all();
 }
 
+// Odd CTAs: tell the pair's MMA-issuing CTA when this CTA's share of a tile
+// has landed (whole warp).
+__device__ void relay(const Params& p, Ctl* c, uint32_t leader, int cluster_id, int n_clusters) {
+  int j = 0;
+  for_items(p, cluster_id, n_clusters, [&](int64_t, const Item& it) {
+    for (int t = it.t0; t < it.t1; ++t, ++j) {
+      const int s = j % kStages;
+      if (!wait_warp(&c->full[s], (uint32_t)(j / kStages) & 1u, c, kSiteRelay, j)) return false;
+      fence_proxy_async_smem();  // cp.async data, written through the generic proxy, feeds the MMA
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive_cluster_relaxed(&c->full_peer[s], leader);
+    }
+    return true;
+  });
+}
+
+// Score rank 1: forward "softmax loaded S" to rank 0 (one thread).
+__device__ void relay_s_free(const Params& p, Ctl* c, int cluster_id, int n_clusters) {
+  int j = 0;
+  for_items(p, cluster_id, n_clusters, [&](int64_t, const Item& it) {
+    for (int t = it.t0; t < it.t1; ++t, ++j) {
+      if (!wait(&c->s_free[j & 1], (uint32_t)(j >> 1) & 1u, c, kSiteSFreeRelay, j)) return false;
+      mbar_arrive_cluster_relaxed(&c->s_free[j & 1], 0);
+    }
+    return true;
+  });
+}
+
 // ---------------------------------------------------------------------------
-// score CTA roles
+// score pair
 // ---------------------------------------------------------------------------
 __device__ void score_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id, int n_clusters) {
-  // run by the whole warp; one elected lane issues each tcgen05 op
+  // rank 0, whole warp; one elected lane issues each pair MMA
   const uint32_t tS = c->tmem_base;        // columns [0, 128): two S buffers
   const uint32_t tQ = c->tmem_base + 128;  // columns [128, 416): queries, bf16 pairs
   int j = 0, seg = 0;
-  bool ok = true;
-  for (int64_t item = cluster_id; item < p.n_items && ok; item += n_clusters) {
-    const Item it = item_at(p, item);
-    if (it.t1 <= it.t0) continue;
-    if (!(ok = wait_warp(&c->q_ready, (uint32_t)seg & 1u, c, kSiteQReady, j))) break;
+  for_items(p, cluster_id, n_clusters, [&](int64_t, const Item& it) {
+    if (!wait_warp(&c->q_ready, (uint32_t)seg & 1u, c, kSiteQReady, j)) return false;
     tc_fence_after();
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       const int s = j % kStages, sb = j & 1;
-      if (!(ok = wait_warp(&c->full[s], (uint32_t)(j / kStages) & 1u, c, kSiteFullS, j))) break;
+      const uint32_t ph = (uint32_t)(j / kStages) & 1u;
+      if (!wait_warp(&c->full[s], ph, c, kSiteFullS, j)) return false;
+      if (!wait_warp(&c->full_peer[s], ph, c, kSitePeer, j)) return false;
       // Issue S(j) only after the softmax has loaded S(j-1): a TMEM load waits
       // behind MMAs issued before it, so issuing S(j) first would hold the
       // softmax's load of S(j-1) until S(j) completes.  (This also implies
       // buffer sb, last read for S(j-2), is free.)
-      if (j > 0 && !(ok = wait_warp(&c->s_free[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c, kSiteSFree, j)))
-        break;
-      fence_proxy_async_smem();  // cp.async data, written through the generic proxy, feeds the MMA
+      if (j > 0 && !wait_warp(&c->s_free[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c, kSiteSFree, j))
+        return false;
+      fence_proxy_async_smem();
       tc_fence_after();
       // descriptors differ only in the start-address field: add (offset >> 4)
-      const uint64_t dk = smem_desc(smem_u32(smem + kOffKvc + s * kKvcStage), 16, 1024, kLayoutSw128);
-      const uint64_t dp = smem_desc(smem_u32(smem + kOffKpe + s * kKpeBytes), 16, 1024, kLayoutSw128);
+      const uint64_t dk = smem_desc(smem_u32(smem + s * kStageS), 16, 1024, kLayoutSw128);
       const uint32_t ts = tS + sb * kTK;
 #pragma unroll
       for (int kc = 0; kc < 9; ++kc) {
-        // chunks 0-7: the latent part in the kv_c stage; chunk 8: the rope part in the k_pe stage
-        const uint64_t bd = kc < 8 ? dk + (uint64_t)((kc * kChunk) >> 4) : dp;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_ts_warp(ts, tQ + kc * 32 + kk * 8, bd + (uint64_t)((kk * 32) >> 4), kIdescS, (kc | kk) != 0);
+          mma_pair_ts_warp(ts, tQ + kc * 32 + kk * 8, dk + (uint64_t)((kc * kChunkS + kk * 32) >> 4), kIdescS,
+                           (kc | kk) != 0);
       }
-      mma_commit_warp(&c->s_full[sb]);
-      mma_commit_warp(&c->empty[s]);
+      mma_pair_commit_warp(&c->s_full[sb], 0x3);
+      mma_pair_commit_warp(&c->empty[s], 0x3);
     }
     ++seg;
-  }
+    return true;
+  });
   if (__any_sync(0xffffffffu, c->abort != 0)) {
     // outstanding S MMAs must finish before TMEM is released
-    mma_commit_warp(&c->drain);
+    mma_pair_commit_warp(&c->drain, 0x1);
     if ((threadIdx.x & 31) == 0) mbar_wait_drain(&c->drain, 0, kDrainLimitNs);
     __syncwarp();
   }
 }
 
-__device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluster_id, int n_clusters) {
+__device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, uint32_t rank, int cluster_id,
+                              int n_clusters) {
+  const int lane = threadIdx.x & 31;
   const int wq = (threadIdx.x >> 5) & 3;            // TMEM lane quadrant of this warp
-  const int r = wq * 32 + (threadIdx.x & 31);        // row within the item
+  const int r = wq * 32 + lane;                      // row within the CTA
   const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
   const uint32_t tS = c->tmem_base + lane_off;
   const uint32_t tQ = c->tmem_base + 128 + lane_off;
+  const uint32_t partner = rank + 2;                 // value CTA of these rows
   const float sl2 = p.scale_log2;
   const int nq = p.Q;
   int j = 0, seg = 0;
-  for (int64_t item = cluster_id; item < p.n_items; item += n_clusters) {
-    const Item it = item_at(p, item);
-    if (it.t1 <= it.t0) continue;
+  for_items(p, cluster_id, n_clusters, [&](int64_t, const Item& it) {
     const int b = it.b;
-    const int row = it.g * kRG + r;
+    const int row = it.g * kRG + (int)rank * kRC + r;
     const bool live = row < p.rows;
     const int64_t P = p.prefix_lens[b];
     const uint64_t anc = live ? p.anc[(int64_t)b * p.Q + row / p.H] : 0ull;
@@ -318,7 +383,8 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&c->q_ready);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_relaxed(&c->q_ready, 0);
     }
 
     // m: running max of the scaled scores (base-2 units); l: running sum of
@@ -326,14 +392,17 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
     float m = -INFINITY, l = 0.f;
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       const int sb = j & 1;
-      if (!wait(&c->s_full[sb], (uint32_t)(j >> 1) & 1u, c, kSiteSFull, j)) return;
-      __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the spin
+      // tcgen05.ld is warp-collective: the warp-uniform wait leaves the warp converged
+      if (!wait_warp(&c->s_full[sb], (uint32_t)(j >> 1) & 1u, c, kSiteSFull, j)) return false;
       tc_fence_after();
       uint32_t u[kTK];
       tmem_ld64_sync(tS + sb * kTK, u);
-      // the tile is in registers: the next S MMA may overwrite this buffer
+      // the tile is in registers: the next S MMA may overwrite this buffer.
+      // A CTA-local arrive: a cluster-scope release here would first wait for
+      // this thread's P stores of the previous tile to reach the value CTA.
       tc_fence_before();
-      mbar_arrive(&c->s_free[sb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c->s_free[sb]);
 
       // prefix + tree mask on the raw scores.  Only tiles reaching the tree
       // tail need it; there the position relative to the first tree node lies
@@ -368,10 +437,10 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
       }
       const float nmu = (m == -INFINITY) ? 0.f : -m;
 
-      // wait until the value CTA is done with this P buffer
-      if (!wait(&c->p_free[sb], ((uint32_t)(j >> 1) & 1u) ^ 1u, c, kSitePFree, j, true)) return;
-      const uint32_t pbase = mapa_shared(smem_u32(smem + kOffP + sb * kPBytes), 1);
-      const uint32_t pbar = mapa_shared(smem_u32(&c->p_full[sb]), 1);
+      // wait until the value partner is done with this P buffer
+      if (!wait_warp(&c->p_free[sb], ((uint32_t)(j >> 1) & 1u) ^ 1u, c, kSitePFree, j)) return false;
+      const uint32_t pbase = mapa_shared(smem_u32(smem + kOffP + sb * kPBytes), partner);
+      const uint32_t pbar = mapa_shared(smem_u32(&c->p_full[sb]), partner);
       // weights 2^(s * scale - m) as bf16, shipped 16 bytes at a time
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -388,193 +457,176 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, int cluste
       }
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       // every row ships its factor; the bytes themselves complete p_full
-      st_async_f32(mapa_shared(smem_u32(&c->alpha[sb][r]), 1), alpha, pbar);
+      st_async_f32(mapa_shared(smem_u32(&c->alpha[sb][r]), partner), alpha, pbar);
     }
 
-    // hand the row statistics to the value CTA for the epilogue
-    if (!wait(&c->fin_free, ((uint32_t)seg & 1u) ^ 1u, c, kSiteFinFree, j, true)) return;
-    st_cluster_f32(mapa_shared(smem_u32(&c->lfin[r]), 1), l);
-    st_cluster_f32(mapa_shared(smem_u32(&c->mfin[r]), 1), m);
-    mbar_arrive_cluster(&c->fin_full, 1);
+    // hand the row statistics to the value partner for the epilogue
+    if (!wait_warp(&c->fin_free, ((uint32_t)seg & 1u) ^ 1u, c, kSiteFinFree, j)) return false;
+    st_cluster_f32(mapa_shared(smem_u32(&c->lfin[r]), partner), l);
+    st_cluster_f32(mapa_shared(smem_u32(&c->mfin[r]), partner), m);
+    mbar_arrive_cluster(&c->fin_full, partner);
     ++seg;
-  }
+    return true;
+  });
 }
 
 // ---------------------------------------------------------------------------
-// value CTA roles
+// value pair
 // ---------------------------------------------------------------------------
 __device__ void value_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id, int n_clusters) {
-  // run by the whole warp; one elected lane issues each tcgen05 op, lane 0
-  // makes the single-count arrivals
+  // rank 2, whole warp; one elected lane issues each pair MMA
   const uint32_t tO = c->tmem_base;
-  const int lane = threadIdx.x & 31;
-  int j = 0, ncmd = 0;
-  bool ok = true;
-  for (int64_t item = cluster_id; item < p.n_items && ok; item += n_clusters) {
-    const Item it = item_at(p, item);
-    if (it.t1 <= it.t0) continue;
+  int j = 0;
+  for_items(p, cluster_id, n_clusters, [&](int64_t, const Item& it) {
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       const int s = j % kStages, pb = j & 1;
-      if (!(ok = wait_warp(&c->full[s], (uint32_t)(j / kStages) & 1u, c, kSiteFullV, j))) break;
-      if (lane == 0) mbar_arrive_expect_tx(&c->p_full[pb], kPTxBytes);
-      if (!(ok = wait_warp(&c->p_full[pb], (uint32_t)(j >> 1) & 1u, c, kSitePFull, j, true))) break;
-      const bool first = (t == it.t0);
-      bool rescale = false;
-      if (!first) {
-        const float4 a = reinterpret_cast<const float4*>(c->alpha[pb])[lane];  // 4 of the 128 rows per lane
-        rescale = __any_sync(0xffffffffu, (a.x != 1.f) | (a.y != 1.f) | (a.z != 1.f) | (a.w != 1.f));
-      }
-      if (rescale) {
-        // O must hold PV(j-1) in full before it is rescaled
-        if (!(ok = wait_warp(&c->pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c, kSitePvPrev, j))) break;
-        tc_fence_after();
-        if (lane == 0) {
-          c->cmd = kCmdRescale;
-          c->cmd_buf = pb;
-          mbar_arrive(&c->cmd_full);
-        }
-        if (!(ok = wait_warp(&c->cmd_done, (uint32_t)ncmd & 1u, c, kSiteCmdDone, j))) break;
-        ++ncmd;
-      }
+      const uint32_t ph = (uint32_t)(j / kStages) & 1u;
+      if (!wait_warp(&c->full[s], ph, c, kSiteFullV, j)) return false;
+      if (!wait_warp(&c->full_peer[s], ph, c, kSitePeer, j)) return false;
+      // P(j) landed in both CTAs and O holds the rescaled PV(0..j-1)
+      if (!wait_warp(&c->o_ready[pb], (uint32_t)(j >> 1) & 1u, c, kSiteOReady, j)) return false;
       fence_proxy_async_smem();
       tc_fence_after();
+      const bool first = (t == it.t0);
       const uint64_t da = smem_desc(smem_u32(smem + kOffP + pb * kPBytes), 16, 1024, kLayoutSw128);
-      const uint64_t dv = smem_desc(smem_u32(smem + kOffKvc + s * kKvcStage), kVAtomStrideN, kVGroupStrideK,
-                                    kLayoutSw128);
+      // V: 64-column atoms 8 KB apart along N, 8-token groups 1 KB apart along K
+      const uint64_t dv = smem_desc(smem_u32(smem + s * kStageV), kAtomV, 1024, kLayoutSw128);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
         for (int nh = 0; nh < 2; ++nh) {
-          mma_ss_warp(tO + nh * 256, da + (uint64_t)((kk * 32) >> 4),
-                      dv + (uint64_t)((nh * 4 * kChunk + kk * 16 * 128) >> 4), kIdescPV, !(first && kk == 0));
+          mma_pair_ss_warp(tO + nh * 256, da + (uint64_t)((kk * 32) >> 4),
+                           dv + (uint64_t)((nh * 2 * kAtomV + kk * 16 * 128) >> 4), kIdescPV, !(first && kk == 0));
         }
       }
-      mma_commit_warp(&c->pv_done[pb]);
-      mma_commit_warp(&c->empty[s]);
+      mma_pair_commit_warp(&c->pv_done[pb], 0xC);
+      mma_pair_commit_warp(&c->empty[s], 0xC);
     }
-    if (!ok) break;
-    // epilogue of this item once its last PV is complete
-    if (!(ok = wait_warp(&c->pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c, kSitePvLast, j))) break;
-    tc_fence_after();
-    if (lane == 0) {
-      c->cmd = kCmdEpilogue;
-      c->cmd_item = item;
-      mbar_arrive(&c->cmd_full);
-    }
-    if (!(ok = wait_warp(&c->cmd_done, (uint32_t)ncmd & 1u, c, kSiteCmdDone, j))) break;
-    ++ncmd;
-  }
-  if (lane == 0) {
-    c->cmd = kCmdExit;
-    mbar_arrive(&c->cmd_full);
-  }
+    return true;
+  });
   if (__any_sync(0xffffffffu, c->abort != 0)) {
     // outstanding PV MMAs must finish before TMEM is released
-    mma_commit_warp(&c->drain);
-    if (lane == 0) mbar_wait_drain(&c->drain, 0, kDrainLimitNs);
-  }
-  __syncwarp();
-}
-
-// Releases each tile's P buffer back to the score CTA once the PV MMAs that
-// read it have completed.
-__device__ void value_release(const Params& p, Ctl* c, int cluster_id, int n_clusters) {
-  int j = 0;
-  for (int64_t item = cluster_id; item < p.n_items; item += n_clusters) {
-    const Item it = item_at(p, item);
-    for (int t = it.t0; t < it.t1; ++t, ++j) {
-      if (!wait(&c->pv_done[j & 1], (uint32_t)(j >> 1) & 1u, c, kSiteRelease, j)) return;
-      mbar_arrive_cluster(&c->p_free[j & 1], 0);
-    }
-  }
-}
-
-__device__ void value_epilogue(const Params& p, Ctl* c) {
-  const int wq = (threadIdx.x >> 5) & 3;
-  const int r = wq * 32 + (threadIdx.x & 31);
-  const uint32_t tO = c->tmem_base + ((uint32_t)(wq * 32) << 16);
-  int ncmd = 0, seg = 0;
-  const float ln2 = 0.69314718055994530942f;
-  while (true) {
-    if (!wait(&c->cmd_full, (uint32_t)ncmd & 1u, c, kSiteCmdFull, ncmd)) return;
+    mma_pair_commit_warp(&c->drain, 0x4);
+    if ((threadIdx.x & 31) == 0) mbar_wait_drain(&c->drain, 0, kDrainLimitNs);
     __syncwarp();
-    ++ncmd;
-    const int cmd = c->cmd;
-    if (cmd == kCmdExit) return;
+  }
+}
+
+// Releases each tile's P buffer back to the score partner once the PV MMAs
+// that read it have completed (one thread).
+__device__ void value_release(const Params& p, Ctl* c, uint32_t rank, int cluster_id, int n_clusters) {
+  int j = 0;
+  for_items(p, cluster_id, n_clusters, [&](int64_t, const Item& it) {
+    for (int t = it.t0; t < it.t1; ++t, ++j) {
+      if (!wait(&c->pv_done[j & 1], (uint32_t)(j >> 1) & 1u, c, kSiteRelease, j)) return false;
+      mbar_arrive_cluster_relaxed(&c->p_free[j & 1], rank - 2);
+    }
+    return true;
+  });
+}
+
+// Row warps of a value CTA: per tile, wait for P, rescale this warp's O rows
+// when a factor differs from 1, and tell the MMA-issuing CTA that O is ready;
+// per item, normalise O and write the outputs (or the split partials).
+__device__ void value_rows(const Params& p, Ctl* c, uint32_t rank, int cluster_id, int n_clusters) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int wq = warp & 3;
+  const int r = wq * 32 + lane;
+  const int half = (int)(rank & 1);
+  const uint32_t tO = c->tmem_base + ((uint32_t)(wq * 32) << 16);
+  const float ln2 = 0.69314718055994530942f;
+  int j = 0, seg = 0;
+  for_items(p, cluster_id, n_clusters, [&](int64_t item, const Item& it) {
+    for (int t = it.t0; t < it.t1; ++t, ++j) {
+      const int pb = j & 1;
+      if (warp == kWarpRows && lane == 0) mbar_arrive_expect_tx(&c->p_full[pb], kPTxBytes);
+      if (!wait_warp(&c->p_full[pb], (uint32_t)(j >> 1) & 1u, c, kSitePFull, j)) return false;
+      if (t != it.t0) {
+        const float a = c->alpha[pb][r];
+        if (__any_sync(0xffffffffu, a != 1.f)) {
+          // O must hold PV(j-1) in full before it is rescaled
+          if (!wait_warp(&c->pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c, kSitePvPrev, j)) return false;
+          tc_fence_after();
+          // warp-collective TMEM traffic: every row takes part (factor 1 = unchanged)
+#pragma unroll 1
+          for (int c0 = 0; c0 < kDl; c0 += 32) {
+            uint32_t u[32];
+            tmem_ld32_sync(tO + c0, u);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) u[q] = __float_as_uint(__uint_as_float(u[q]) * a);
+            tmem_st_32x32b_x32(tO + c0, u);
+          }
+          tmem_wait_st();
+        }
+      }
+      fence_proxy_async_smem();  // the P bytes feed the MMA
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_relaxed(&c->o_ready[pb], 2);
+    }
+
+    // epilogue of this item once its last PV is complete
+    if (!wait_warp(&c->pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c, kSitePvLast, j)) return false;
+    if (!wait_warp(&c->fin_full, (uint32_t)seg & 1u, c, kSiteFinFull, seg)) return false;
     tc_fence_after();
-    if (cmd == kCmdRescale) {
-      // warp-collective TMEM traffic: every row takes part (factor 1 = unchanged)
-      const float a = c->alpha[c->cmd_buf][r];
+    const float l = c->lfin[r], m = c->mfin[r];
+    mbar_arrive_cluster_relaxed(&c->fin_free, rank - 2);
+    ++seg;
+    const int row = it.g * kRG + half * kRC + r;
+    const bool live = row < p.rows;  // TMEM loads stay warp-wide; only stores are per row
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float lse = l > 0.f ? (m + log2f(l)) * ln2 : -INFINITY;
+    const int64_t orow = (int64_t)it.b * p.rows + row;
+    if (p.splits == 1) {
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDl);
 #pragma unroll 1
       for (int c0 = 0; c0 < kDl; c0 += 32) {
         uint32_t u[32];
+        __syncwarp();
         tmem_ld32_sync(tO + c0, u);
+        if (live) {
 #pragma unroll
-        for (int q = 0; q < 32; ++q) u[q] = __float_as_uint(__uint_as_float(u[q]) * a);
-        tmem_st_32x32b_x32(tO + c0, u);
-      }
-      tmem_wait_st();
-    } else {  // kCmdEpilogue
-      const Item it = item_at(p, c->cmd_item);
-      if (!wait(&c->fin_full, (uint32_t)seg & 1u, c, kSiteFinFull, seg, true)) return;
-      __syncwarp();
-      const float l = c->lfin[r], m = c->mfin[r];
-      mbar_arrive_cluster(&c->fin_free, 0);
-      ++seg;
-      const int row = it.g * kRG + r;
-      const bool live = row < p.rows;  // TMEM loads stay warp-wide; only stores are per row
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const float lse = l > 0.f ? (m + log2f(l)) * ln2 : -INFINITY;
-      const int64_t orow = (int64_t)it.b * p.rows + row;
-      if (p.splits == 1) {
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDl);
-#pragma unroll 1
-        for (int c0 = 0; c0 < kDl; c0 += 32) {
-          uint32_t u[32];
-          __syncwarp();
-          tmem_ld32_sync(tO + c0, u);
-          if (live) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 o;
-              o.x = pack_bf16(__uint_as_float(u[8 * v + 0]) * inv, __uint_as_float(u[8 * v + 1]) * inv);
-              o.y = pack_bf16(__uint_as_float(u[8 * v + 2]) * inv, __uint_as_float(u[8 * v + 3]) * inv);
-              o.z = pack_bf16(__uint_as_float(u[8 * v + 4]) * inv, __uint_as_float(u[8 * v + 5]) * inv);
-              o.w = pack_bf16(__uint_as_float(u[8 * v + 6]) * inv, __uint_as_float(u[8 * v + 7]) * inv);
-              dst[c0 / 8 + v] = o;
-            }
+          for (int v = 0; v < 4; ++v) {
+            uint4 o;
+            o.x = pack_bf16(__uint_as_float(u[8 * v + 0]) * inv, __uint_as_float(u[8 * v + 1]) * inv);
+            o.y = pack_bf16(__uint_as_float(u[8 * v + 2]) * inv, __uint_as_float(u[8 * v + 3]) * inv);
+            o.z = pack_bf16(__uint_as_float(u[8 * v + 4]) * inv, __uint_as_float(u[8 * v + 5]) * inv);
+            o.w = pack_bf16(__uint_as_float(u[8 * v + 6]) * inv, __uint_as_float(u[8 * v + 7]) * inv);
+            dst[c0 / 8 + v] = o;
           }
         }
-        if (live && p.lse) p.lse[orow] = lse;
-      } else {
-        const int64_t prow = c->cmd_item * kRG + r;
-        float4* dst = reinterpret_cast<float4*>(p.part_o + prow * kDl);
-#pragma unroll 1
-        for (int c0 = 0; c0 < kDl; c0 += 32) {
-          uint32_t u[32];
-          __syncwarp();
-          tmem_ld32_sync(tO + c0, u);
-          if (live) {
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              dst[c0 / 4 + v] = make_float4(__uint_as_float(u[4 * v + 0]) * inv, __uint_as_float(u[4 * v + 1]) * inv,
-                                            __uint_as_float(u[4 * v + 2]) * inv, __uint_as_float(u[4 * v + 3]) * inv);
-          }
-        }
-        if (live) p.part_lse[prow] = lse;
       }
+      if (live && p.lse) p.lse[orow] = lse;
+    } else {
+      const int64_t prow = item * kRG + half * kRC + r;
+      float4* dst = reinterpret_cast<float4*>(p.part_o + prow * kDl);
+#pragma unroll 1
+      for (int c0 = 0; c0 < kDl; c0 += 32) {
+        uint32_t u[32];
+        __syncwarp();
+        tmem_ld32_sync(tO + c0, u);
+        if (live) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[c0 / 4 + v] = make_float4(__uint_as_float(u[4 * v + 0]) * inv, __uint_as_float(u[4 * v + 1]) * inv,
+                                          __uint_as_float(u[4 * v + 2]) * inv, __uint_as_float(u[4 * v + 3]) * inv);
+        }
+      }
+      if (live) p.part_lse[prow] = lse;
     }
+    // the next item's first PV overwrites O: its o_ready follows these loads
     tc_fence_before();
-    mbar_arrive(&c->cmd_done);
-  }
+    return true;
+  });
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_tc_kernel(const Params p) {
+__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads, 1) attn_tc_kernel(const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
   const uint32_t rank = cluster_ctarank();
   const int warp = threadIdx.x >> 5;
-  // Both CTAs of a cluster must take the same branch here.  The validation bits
+  // All CTAs of a cluster must take the same branch here.  The validation bits
   // were final before this kernel started; the timeout bit may be raised by
   // another cluster while this one starts, so it is not part of the test.
   if ((*p.err & ~MLA_DEVERR_TIMEOUT) || (smem_u32(smem) & 1023u)) {
@@ -585,44 +637,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_tc
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&c->full[s], kProducerThreads);
+      mbar_init(&c->full_peer[s], 1);
       mbar_init(&c->empty[s], 1);
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(&c->s_full[q], 1);
-      mbar_init(&c->s_free[q], kRG);
+      mbar_init(&c->s_free[q], rank == 0 ? 5 : 4);
       mbar_init(&c->p_free[q], 1);
       mbar_init(&c->p_full[q], 1);
       mbar_init(&c->pv_done[q], 1);
+      mbar_init(&c->o_ready[q], 8);
     }
-    mbar_init(&c->q_ready, kRG);
-    mbar_init(&c->fin_free, kRG);
-    mbar_init(&c->fin_full, kRG);
-    mbar_init(&c->cmd_full, 1);
-    mbar_init(&c->cmd_done, kRG);
+    mbar_init(&c->q_ready, 8);
+    mbar_init(&c->fin_free, kRC);
+    mbar_init(&c->fin_full, kRC);
     mbar_init(&c->drain, 1);
     c->abort = 0;
     c->abort_site = 0;
     fence_mbar_init();
   }
   if (warp == kWarpTmem) {
-    tmem_alloc(&c->tmem_base, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(&c->tmem_base, kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  cluster_sync();  // barriers of both CTAs initialised before any remote use
+  cluster_sync();  // barriers of all CTAs initialised before any remote use
   tc_fence_after();
 
-  const int cluster_id = blockIdx.x >> 1;
-  const int n_clusters = gridDim.x >> 1;
+  const int cluster_id = blockIdx.x / kClusterCtas;
+  const int n_clusters = gridDim.x / kClusterCtas;
+  const bool score = rank < 2, leader = (rank & 1) == 0;
   if (warp < kProducerWarps) {
-    producer(p, smem, c, warp, rank == 0, cluster_id, n_clusters);
-  } else if (rank == 0) {
-    if (warp == kWarpMma) score_mma(p, smem, c, cluster_id, n_clusters);
-    else if (warp >= kWarpRows) score_softmax(p, smem, c, cluster_id, n_clusters);
-  } else {
-    if (warp == kWarpMma) value_mma(p, smem, c, cluster_id, n_clusters);
-    else if (warp == kWarpRelease) { if ((threadIdx.x & 31) == 0) value_release(p, c, cluster_id, n_clusters); }
-    else if (warp >= kWarpRows) value_epilogue(p, c);
+    producer(p, smem, c, warp, rank, cluster_id, n_clusters);
+  } else if (warp == kWarpMma) {
+    if (!leader) relay(p, c, rank & 2u, cluster_id, n_clusters);
+    else if (score) score_mma(p, smem, c, cluster_id, n_clusters);
+    else value_mma(p, smem, c, cluster_id, n_clusters);
+  } else if (warp == kWarpRelease) {
+    if ((threadIdx.x & 31) == 0) {
+      if (!score) value_release(p, c, rank, cluster_id, n_clusters);
+      else if (!leader) relay_s_free(p, c, cluster_id, n_clusters);
+    }
+  } else if (warp >= kWarpRows) {
+    if (score) score_softmax(p, smem, c, rank, cluster_id, n_clusters);
+    else value_rows(p, c, rank, cluster_id, n_clusters);
   }
 
   __syncwarp();
@@ -630,12 +688,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_tc
   __syncthreads();
   if (threadIdx.x == 0 && c->abort) {
     set_err(p.err, MLA_DEVERR_TIMEOUT);
-    atomicCAS(p.err + 1, 0u, (uint32_t)c->abort_site | (rank << 8));
+    if (c->abort_site) atomicCAS(p.err + 1, 0u, (uint32_t)c->abort_site | (rank << 8));
   }
   __syncthreads();
   tc_fence_after();
-  cluster_sync();  // no CTA leaves while its peer may still touch its shared memory
-  if (warp == kWarpTmem) tmem_dealloc(c->tmem_base, kTmemCols);
+  cluster_sync();  // no CTA leaves while a peer may still touch its shared memory
+  if (warp == kWarpTmem) tmem_dealloc_pair(c->tmem_base, kTmemCols);
 }
 
 }  // namespace tc
@@ -644,19 +702,19 @@ int tc_rows_per_group() { return tc::kRG; }
 int tc_tokens_per_tile() { return tc::kTK; }
 int tc_default_for(int dtype) { return dtype == MLA_BF16 ? MLA_ALGO_TC : MLA_ALGO_SIMT; }
 
-// Clusters of two CTAs that can be resident at once (one CTA per SM).
+// Clusters of four CTAs that can be resident at once (one CTA per SM).
 int tc_clusters_per_gpu(int sm_count) {
   static int cached = -1;
   if (cached > 0) return cached;
   cudaFuncSetAttribute(tc::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemAlloc);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * (sm_count / 2), 1, 1);
+  cfg.gridDim = dim3(tc::kClusterCtas * (sm_count / tc::kClusterCtas), 1, 1);
   cfg.blockDim = dim3(tc::kThreads, 1, 1);
   cfg.dynamicSmemBytes = tc::kSmemAlloc;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, tc::attn_tc_kernel, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
-    n = sm_count / 2;
+    n = sm_count / tc::kClusterCtas;
   }
   cached = n;
   return n;
@@ -666,7 +724,7 @@ cudaError_t launch_attn_tc(const Params& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(tc::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        tc::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  tc::attn_tc_kernel<<<2 * p.grid, tc::kThreads, tc::kSmemAlloc, stream>>>(p);
+  tc::attn_tc_kernel<<<tc::kClusterCtas * p.grid, tc::kThreads, tc::kSmemAlloc, stream>>>(p);
   return cudaGetLastError();
 }
 
