@@ -66,17 +66,21 @@ namespace tc {
 constexpr int kRG = 256;        // query rows per work item (pair MMA M)
 constexpr int kRC = 128;        // query rows per CTA
 constexpr int kTK = 64;         // tokens per KV tile (S MMA N)
-constexpr int kStages = 6;      // KV tiles in flight
-constexpr int kThreads = 512;   // 16 warps
+constexpr int kStagesS = 5;     // KV tiles in flight, score pair
+constexpr int kStagesV = 6;     // KV tiles in flight, value pair
+constexpr int kStagesMax = kStagesV;
+constexpr int kThreads = 576;   // 18 warps
 constexpr int kClusterCtas = 4;
 constexpr uint32_t kTmemCols = 512;
 
 // warp roles
 constexpr int kProducerWarps = 8;  // warps 0-7
 constexpr int kProducerThreads = 32 * kProducerWarps;
-constexpr int kWarpMma = 8;        // MMA issue (even CTAs) or tile-landed relay (odd CTAs)
-constexpr int kWarpRelease = 9;    // value: P release; score rank 1: s_free relay
-constexpr int kWarpTmem = 10, kWarpRows = 12;  // rows: 12-15
+// Row warps 8-15: two warpgroups, each covering the CTA's 128 rows (warp w
+// reaches TMEM lanes 32 (w % 4) ..); warpgroup h takes columns half h.
+constexpr int kWarpRows = 8, kRowWarps = 8, kRowThreads = 32 * kRowWarps;
+constexpr int kWarpMma = 16;  // MMA issue (even CTAs) or tile-landed relay (odd CTAs)
+constexpr int kWarpAux = 17;  // TMEM allocation; lane 0: P bulk copies (score CTAs), P release (value CTAs)
 
 // score CTA stage: its 32 tokens x 576 columns, as 9 chunks of 64 columns
 // (chunks 0-7 kv_c, chunk 8 k_pe), each chunk 32 rows of 128 bytes
@@ -89,9 +93,17 @@ constexpr int kStageS = 9 * kChunkS;                  // 36 KB
 constexpr int kTokVPerWarp = kTK / kProducerWarps;  // 8
 constexpr int kAtomV = kTK * 128;                   // 8 KB
 constexpr int kStageV = 4 * kAtomV;                 // 32 KB
-constexpr int kOffP = kStages * kStageV;            // value CTA: [2][16 KB]
+constexpr int kOffP = kStagesV * kStageV;           // value CTA: [2][16 KB]
 constexpr int kPBytes = kRC * 128;                  // P tile [128 rows x 64 tokens] bf16
 constexpr int kOffCtl = kOffP + 2 * kPBytes;
+// score CTA, after its stages: P and its rescale factors are staged here
+// ([2][16 KB], [2][128] floats) and bulk-copied to the value CTA; then the
+// partial row maxima the two column halves of a row exchange per tile
+// ([2 tiles][2 halves][128 rows]) and the partial sums per item ([128])
+constexpr int kOffPStage = kStagesS * kStageS;
+constexpr int kOffAStage = kOffPStage + 2 * kPBytes;
+constexpr int kOffRed = kOffAStage + 2 * kRC * 4;
+constexpr int kRedBytes = (2 * 2 * kRC + kRC) * 4;
 constexpr uint32_t kPTxBytes = kPBytes + kRC * 4;   // P tile + alpha, per tile
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(kRG, kTK, 0, 0);  // A (Q, TMEM), B (K tile) K-major
@@ -101,20 +113,23 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 20000000ull;   // 20 ms per drain wait on abort
 
 struct alignas(16) Ctl {
-  uint64_t full[kStages];       // this CTA's share of a tile landed (kProducerThreads cp.async arrivals)
-  uint64_t full_peer[kStages];  // even CTAs: the odd CTA's share landed (1 relayed arrival)
-  uint64_t empty[kStages];      // stage reusable: the pair MMAs reading it are complete
+  uint64_t full[kStagesMax];       // this CTA's share of a tile landed (kProducerThreads cp.async arrivals;
+                                // even CTAs: + 1 relayed arrival for the odd CTA's share)
+  uint64_t empty[kStagesMax];      // stage reusable: the pair MMAs reading it are complete
   uint64_t s_full[2];           // score: S tile in TMEM
-  uint64_t s_free[2];           // score: this CTA's softmax warps loaded S (4 warp arrivals; rank 0: +1 relayed)
-  uint64_t q_ready;             // score, rank 0: both CTAs' queries in TMEM (8 warp arrivals)
+  uint64_t s_free[2];           // score, rank 0: both CTAs' softmax warps loaded S (16 warp arrivals)
+  uint64_t q_ready;             // score, rank 0: both CTAs' queries in TMEM (16 warp arrivals)
   uint64_t p_free[2];           // score: the value partner finished with its P buffer
-  uint64_t fin_free;            // score: the value partner consumed lfin/mfin (128 arrivals)
+  uint64_t fin_free;            // score: the value partner consumed lfin/mfin (256 arrivals)
+  uint64_t xch[2];              // score: both halves' partial row maxima of a tile written (8 warp arrivals)
+  uint64_t xfin;                // score: half 1's partial row sums of an item written (4 warp arrivals)
+  uint64_t p_staged[2];         // score: P and alpha of a tile staged locally (8 warp arrivals)
   uint64_t p_full[2];           // value: P tile and alpha landed (st.async bytes; armed by a row thread)
   uint64_t pv_done[2];          // value: PV MMAs of a tile complete
-  uint64_t o_ready[2];          // value, rank 2: both CTAs' O ready for the tile's PV (8 warp arrivals)
+  uint64_t o_ready[2];          // value, rank 2: both CTAs' O ready for the tile's PV (16 warp arrivals)
   uint64_t fin_full;            // value: lfin/mfin written (128 remote arrivals)
   uint64_t drain;               // even CTAs: final MMA drain on abort
-  float alpha[2][kRC];          // value: per-row rescale of O before PV(j) (1 = unchanged)
+  alignas(16) float alpha[2][kRC];  // value: per-row rescale of O before PV(j) (1 = unchanged; bulk-copy target)
   float lfin[kRC];              // value: final row sums of the weights
   float mfin[kRC];              // value: final running max (base-2 units)
   uint32_t tmem_base;
@@ -122,16 +137,19 @@ struct alignas(16) Ctl {
   int abort_site;
 };
 constexpr int kSmemBytes = kOffCtl + (int)sizeof(Ctl);
+static_assert(offsetof(Ctl, alpha) % 16 == 0, "bulk-copy target alignment");
 constexpr int kSmemAlloc = 232448;  // the per-CTA maximum; the base must be 1024-aligned
 static_assert(kSmemBytes <= kSmemAlloc, "shared memory budget");
-static_assert(kStages * kStageS <= kOffCtl, "score stages overlap the control block");
-static_assert(kWarpRows % 4 == 0, "the row warps must form a warpgroup (TMEM lane quadrants)");
+static_assert(kOffRed + kRedBytes <= kOffCtl, "score stages overlap the control block");
+static_assert(kOffPStage % 1024 == 0 && kOffAStage % 16 == 0, "staging buffers: swizzle atoms and bulk-copy alignment");
+static_assert(kWarpRows % 4 == 0 && kRowWarps == 8, "the row warps must form two warpgroups (TMEM lane quadrants)");
+static_assert(kWarpAux < kThreads / 32, "warp roles exceed the CTA");
 
 // Wait sites, recorded in the workspace's second error word when a wait gives up.
 enum {
   kSiteEmpty = 1, kSiteQReady, kSiteFullS, kSiteSFree, kSiteSFull, kSitePFree, kSiteFinFree,
   kSiteFullV, kSiteOReady, kSitePFull, kSitePvPrev, kSitePvLast, kSiteRelease, kSiteRelay, kSiteFinFull,
-  kSitePeer, kSiteSFreeRelay
+  kSiteXch, kSitePStaged
 };
 
 // Bounded wait on a barrier of this CTA.  Barriers that other CTAs (or pair
@@ -197,6 +215,7 @@ __device__ void producer(const Params& p, uint8_t* smem, Ctl* c, int pw, uint32_
   const bool score = rank < 2;
   const int half = (int)(rank & 1);
   const int ntok = score ? kTokSPerWarp : kTokVPerWarp;
+  const int nst = score ? kStagesS : kStagesV;
   const int r0 = ntok * pw;                  // first token row of this warp within the CTA's share
   const int tok0 = score ? half * kTokS : 0;  // the share's first token within the tile
   const __nv_bfloat16* kvc_g = reinterpret_cast<const __nv_bfloat16*>(p.kv_c);
@@ -222,11 +241,11 @@ __device__ void producer(const Params& p, uint8_t* smem, Ctl* c, int pw, uint32_
     };
     int64_t next = slot_of(it.t0);
     for (int t = it.t0; t < it.t1; ++t, ++j) {
-      const int s = j % kStages;
+      const int s = j % nst;
       const int64_t slot = next;
       if (t + 1 < it.t1) next = slot_of(t + 1);  // index load for the next tile, in flight meanwhile
       bool ok = true;
-      if (lane == 0) ok = wait(&c->empty[s], ((uint32_t)(j / kStages) & 1u) ^ 1u, c, kSiteEmpty, j);
+      if (lane == 0) ok = wait(&c->empty[s], ((uint32_t)(j / nst) & 1u) ^ 1u, c, kSiteEmpty, j);
       if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
       if (score) {
         const uint32_t stage = sbase + s * kStageS;
@@ -269,26 +288,15 @@ __device__ void producer(const Params& p, uint8_t* smem, Ctl* c, int pw, uint32_
 // Odd CTAs: tell the pair's MMA-issuing CTA when this CTA's share of a tile
 // has landed (whole warp).
 __device__ void relay(const Params& p, Ctl* c, uint32_t leader, int cluster_id, int n_clusters) {
+  const int nst = leader == 0 ? kStagesS : kStagesV;
   int j = 0;
   for_items(p, cluster_id, n_clusters, [&](int64_t, const Item& it) {
     for (int t = it.t0; t < it.t1; ++t, ++j) {
-      const int s = j % kStages;
-      if (!wait_warp(&c->full[s], (uint32_t)(j / kStages) & 1u, c, kSiteRelay, j)) return false;
+      const int s = j % nst;
+      if (!wait_warp(&c->full[s], (uint32_t)(j / nst) & 1u, c, kSiteRelay, j)) return false;
       fence_proxy_async_smem();  // cp.async data, written through the generic proxy, feeds the MMA
       __syncwarp();
-      if ((threadIdx.x & 31) == 0) mbar_arrive_cluster_relaxed(&c->full_peer[s], leader);
-    }
-    return true;
-  });
-}
-
-// Score rank 1: forward "softmax loaded S" to rank 0 (one thread).
-__device__ void relay_s_free(const Params& p, Ctl* c, int cluster_id, int n_clusters) {
-  int j = 0;
-  for_items(p, cluster_id, n_clusters, [&](int64_t, const Item& it) {
-    for (int t = it.t0; t < it.t1; ++t, ++j) {
-      if (!wait(&c->s_free[j & 1], (uint32_t)(j >> 1) & 1u, c, kSiteSFreeRelay, j)) return false;
-      mbar_arrive_cluster_relaxed(&c->s_free[j & 1], 0);
+      if ((threadIdx.x & 31) == 0) mbar_arrive_cluster_relaxed(&c->full[s], leader);
     }
     return true;
   });
@@ -298,24 +306,31 @@ __device__ void relay_s_free(const Params& p, Ctl* c, int cluster_id, int n_clus
 // score pair
 // ---------------------------------------------------------------------------
 __device__ void score_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id, int n_clusters) {
-  // rank 0, whole warp; one elected lane issues each pair MMA
+  // rank 0, whole warp; one elected lane issues each pair MMA.  While the
+  // tensor pipe works through a tile's MMAs, the warp checks (without
+  // blocking) whether the next tile can start, so the checks cost no pipe time.
   const uint32_t tS = c->tmem_base;        // columns [0, 128): two S buffers
   const uint32_t tQ = c->tmem_base + 128;  // columns [128, 416): queries, bf16 pairs
   int j = 0, seg = 0;
+  // S(j) may start once its tile has landed in both CTAs and the softmax has
+  // loaded S(j-2) from buffer j & 1 (the softmax loading S(j-1) from the other
+  // buffer meanwhile does not delay these MMAs: measured, a TMEM load of other
+  // columns completes in tens of cycles while MMAs run)
+  auto ready_test = [&](int jj) {
+    const bool ok = mbar_test_wait_cluster(&c->full[jj % kStagesS], (uint32_t)(jj / kStagesS) & 1u) &&
+                    (jj < 2 || mbar_test_wait_cluster(&c->s_free[jj & 1], (((uint32_t)jj >> 1) & 1u) ^ 1u));
+    return __all_sync(0xffffffffu, ok);
+  };
   for_items(p, cluster_id, n_clusters, [&](int64_t, const Item& it) {
     if (!wait_warp(&c->q_ready, (uint32_t)seg & 1u, c, kSiteQReady, j)) return false;
     tc_fence_after();
+    bool ready = false;
     for (int t = it.t0; t < it.t1; ++t, ++j) {
-      const int s = j % kStages, sb = j & 1;
-      const uint32_t ph = (uint32_t)(j / kStages) & 1u;
-      if (!wait_warp(&c->full[s], ph, c, kSiteFullS, j)) return false;
-      if (!wait_warp(&c->full_peer[s], ph, c, kSitePeer, j)) return false;
-      // Issue S(j) only after the softmax has loaded S(j-1): a TMEM load waits
-      // behind MMAs issued before it, so issuing S(j) first would hold the
-      // softmax's load of S(j-1) until S(j) completes.  (This also implies
-      // buffer sb, last read for S(j-2), is free.)
-      if (j > 0 && !wait_warp(&c->s_free[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, c, kSiteSFree, j))
-        return false;
+      const int s = j % kStagesS, sb = j & 1;
+      if (!ready) {
+        if (!wait_warp(&c->full[s], (uint32_t)(j / kStagesS) & 1u, c, kSiteFullS, j)) return false;
+        if (j >= 2 && !wait_warp(&c->s_free[sb], (((uint32_t)j >> 1) & 1u) ^ 1u, c, kSiteSFree, j)) return false;
+      }
       fence_proxy_async_smem();
       tc_fence_after();
       // descriptors differ only in the start-address field: add (offset >> 4)
@@ -327,6 +342,7 @@ __device__ void score_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id
         for (int kk = 0; kk < 4; ++kk)
           mma_pair_ts_warp(ts, tQ + kc * 32 + kk * 8, dk + (uint64_t)((kc * kChunkS + kk * 32) >> 4), kIdescS,
                            (kc | kk) != 0);
+        if (kc == 5) ready = (t + 1 < it.t1) && ready_test(j + 1);
       }
       mma_pair_commit_warp(&c->s_full[sb], 0x3);
       mma_pair_commit_warp(&c->empty[s], 0x3);
@@ -342,15 +358,24 @@ __device__ void score_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id
   }
 }
 
+// Online softmax of this CTA's 128 rows.  Each row is shared by two threads
+// (warps w and w + 4 of the row warps) that take columns [32 h, 32 h + 32) of
+// every tile: they exchange partial maxima per tile through shared memory, so
+// both follow the same running max, and keep partial row sums that are added
+// once per item.
 __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, uint32_t rank, int cluster_id,
                               int n_clusters) {
   const int lane = threadIdx.x & 31;
-  const int wq = (threadIdx.x >> 5) & 3;            // TMEM lane quadrant of this warp
+  const int w = (threadIdx.x >> 5) - kWarpRows;     // 0..7
+  const int wq = w & 3;                              // TMEM lane quadrant of this warp
+  const int h = w >> 2;                              // column half
   const int r = wq * 32 + lane;                      // row within the CTA
   const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-  const uint32_t tS = c->tmem_base + lane_off;
+  const uint32_t tS = c->tmem_base + lane_off + (uint32_t)(h * 32);
   const uint32_t tQ = c->tmem_base + 128 + lane_off;
-  const uint32_t partner = rank + 2;                 // value CTA of these rows
+  const uint32_t partner = rank + 2;                 // value CTA of these rows (row statistics)
+  float* red_max = reinterpret_cast<float*>(smem + kOffRed);  // [2][2][kRC]
+  float* red_l = red_max + 4 * kRC;                            // [kRC]
   const float sl2 = p.scale_log2;
   const int nq = p.Q;
   int j = 0, seg = 0;
@@ -361,25 +386,26 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, uint32_t r
     const int64_t P = p.prefix_lens[b];
     const uint64_t anc = live ? p.anc[(int64_t)b * p.Q + row / p.H] : 0ull;
 
-    // stage this item's queries into TMEM: column c holds elements 2c, 2c+1
+    // stage this item's queries into TMEM (half h: columns [144 h, 144 h + 144));
+    // column c holds elements 2c, 2c+1
     {
       const uint4* ql = reinterpret_cast<const uint4*>(p.q_lat) + ((int64_t)b * p.rows + row) * (kDl / 8);
       const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe) + ((int64_t)b * p.rows + row) * (kDr / 8);
 #pragma unroll 1
-      for (int c0 = 0; c0 < 288; c0 += 16) {
-        uint32_t w[16];
+      for (int c0 = 144 * h; c0 < 144 * h + 144; c0 += 16) {
+        uint32_t wv[16];
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const int col = c0 + 4 * v;  // 4 columns per 16-byte vector
           uint4 x = make_uint4(0, 0, 0, 0);
           if (live) x = col < 256 ? ql[col / 4] : qp[(col - 256) / 4];
-          w[4 * v + 0] = x.x;
-          w[4 * v + 1] = x.y;
-          w[4 * v + 2] = x.z;
-          w[4 * v + 3] = x.w;
+          wv[4 * v + 0] = x.x;
+          wv[4 * v + 1] = x.y;
+          wv[4 * v + 2] = x.z;
+          wv[4 * v + 3] = x.w;
         }
         __syncwarp();
-        tmem_st_32x32b_x16(tQ + c0, w);
+        tmem_st_32x32b_x16(tQ + c0, wv);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -387,47 +413,53 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, uint32_t r
       if (lane == 0) mbar_arrive_cluster_relaxed(&c->q_ready, 0);
     }
 
-    // m: running max of the scaled scores (base-2 units); l: running sum of
-    // the weights 2^(score - m), accumulated in fp32 before bf16 rounding
+    // m: running max of the scaled scores (base-2 units), the same in both
+    // halves; l: this half's running sum of the weights 2^(score - m),
+    // accumulated in fp32 before bf16 rounding
     float m = -INFINITY, l = 0.f;
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       const int sb = j & 1;
       // tcgen05.ld is warp-collective: the warp-uniform wait leaves the warp converged
       if (!wait_warp(&c->s_full[sb], (uint32_t)(j >> 1) & 1u, c, kSiteSFull, j)) return false;
       tc_fence_after();
-      uint32_t u[kTK];
-      tmem_ld64_sync(tS + sb * kTK, u);
-      // the tile is in registers: the next S MMA may overwrite this buffer.
-      // A CTA-local arrive: a cluster-scope release here would first wait for
-      // this thread's P stores of the previous tile to reach the value CTA.
+      uint32_t u[32];
+      tmem_ld32_sync(tS + sb * kTK, u);
+      // the tile is in registers: the next S MMA may overwrite this buffer
+      // (relaxed: a release arrive would first wait for this thread's P
+      // stores of the previous tile to reach the value CTA)
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&c->s_free[sb]);
+      if (lane == 0) mbar_arrive_cluster_relaxed(&c->s_free[sb], 0);
 
       // prefix + tree mask on the raw scores.  Only tiles reaching the tree
       // tail need it; there the position relative to the first tree node lies
       // in (-64, Q + 64).  The branch is uniform across the warp (one tile,
       // one sequence), so it sits outside the loop.
-      const int64_t pos0 = (int64_t)t * kTK;
-      if (pos0 + kTK > P) {
+      const int64_t pos0 = (int64_t)t * kTK + 32 * h;
+      if (pos0 + 32 > P) {
         const int rel0 = (int)(pos0 - P);
 #pragma unroll
-        for (int q = 0; q < kTK; ++q) {
+        for (int q = 0; q < 32; ++q) {
           const int rel = rel0 + q;  // < 0: prefix; [0, Q): tree node rel
           const bool vis = rel < 0 || (rel < nq && ((anc >> (rel & 63)) & 1ull));
           if (!vis) u[q] = 0xff800000u;  // -inf
         }
       }
-      // row max of the raw scores in eight independent chains; the scale is
-      // positive, so scaling the max equals the max of the scaled scores
-      float mx[8];
+      // partial row max of the raw scores in four independent chains
+      float mx[4];
 #pragma unroll
-      for (int v = 0; v < 8; ++v) mx[v] = __uint_as_float(u[v]);
+      for (int v = 0; v < 4; ++v) mx[v] = __uint_as_float(u[v]);
 #pragma unroll
-      for (int q = 8; q < kTK; ++q) mx[q & 7] = fmaxf(mx[q & 7], __uint_as_float(u[q]));
-      const float tmax =
-          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
-          sl2;
+      for (int q = 4; q < 32; ++q) mx[q & 3] = fmaxf(mx[q & 3], __uint_as_float(u[q]));
+      const float pmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      // exchange with the other half of the row
+      red_max[((j & 1) * 2 + h) * kRC + r] = pmax;
+      __threadfence_block();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c->xch[j & 1]);
+      if (!wait_warp(&c->xch[j & 1], (uint32_t)(j >> 1) & 1u, c, kSiteXch, j)) return false;
+      // the scale is positive, so scaling the max equals the max of the scaled scores
+      const float tmax = fmaxf(pmax, red_max[((j & 1) * 2 + (h ^ 1)) * kRC + r]) * sl2;
       // lazy running max: move it only when this tile beats it by > 8 (x 2^8)
       float alpha = 1.f;
       if (tmax > m + 8.f) {
@@ -437,54 +469,94 @@ __device__ void score_softmax(const Params& p, uint8_t* smem, Ctl* c, uint32_t r
       }
       const float nmu = (m == -INFINITY) ? 0.f : -m;
 
-      // wait until the value partner is done with this P buffer
+      // wait until the value partner is done with this P buffer (and so with
+      // the local staging buffer the bulk copy read it from)
       if (!wait_warp(&c->p_free[sb], ((uint32_t)(j >> 1) & 1u) ^ 1u, c, kSitePFree, j)) return false;
-      const uint32_t pbase = mapa_shared(smem_u32(smem + kOffP + sb * kPBytes), partner);
-      const uint32_t pbar = mapa_shared(smem_u32(&c->p_full[sb]), partner);
-      // weights 2^(s * scale - m) as bf16, shipped 16 bytes at a time
+      uint8_t* pst = smem + kOffPStage + sb * kPBytes;
+      // weights 2^(s * scale - m) as bf16, staged in the swizzled operand layout
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int q8 = 0; q8 < kTK / 8; ++q8) {
-        uint32_t w[4];
+      for (int q8 = 0; q8 < 4; ++q8) {
+        uint32_t wv[4];
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const float e0 = ex2_approx(fmaf(__uint_as_float(u[8 * q8 + 2 * v]), sl2, nmu));
           const float e1 = ex2_approx(fmaf(__uint_as_float(u[8 * q8 + 2 * v + 1]), sl2, nmu));
           ls[v] += e0 + e1;
-          w[v] = pack_bf16(e0, e1);
+          wv[v] = pack_bf16(e0, e1);
         }
-        st_async_v4(pbase + sw128_offset(r, 8 * q8), w[0], w[1], w[2], w[3], pbar);
+        *reinterpret_cast<uint4*>(pst + sw128_offset(r, 32 * h + 8 * q8)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
       }
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      // every row ships its factor; the bytes themselves complete p_full
-      st_async_f32(mapa_shared(smem_u32(&c->alpha[sb][r]), partner), alpha, pbar);
+      if (h == 0) reinterpret_cast<float*>(smem + kOffAStage)[sb * kRC + r] = alpha;  // one factor per row
+      // the staged bytes are read by the bulk-copy engine (async proxy)
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c->p_staged[sb]);
     }
 
-    // hand the row statistics to the value partner for the epilogue
-    if (!wait_warp(&c->fin_free, ((uint32_t)seg & 1u) ^ 1u, c, kSiteFinFree, j)) return false;
-    st_cluster_f32(mapa_shared(smem_u32(&c->lfin[r]), partner), l);
-    st_cluster_f32(mapa_shared(smem_u32(&c->mfin[r]), partner), m);
-    mbar_arrive_cluster(&c->fin_full, partner);
+    // add the halves' row sums and hand the statistics to the value partner
+    if (h == 1) {
+      red_l[r] = l;
+      __threadfence_block();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c->xfin);
+    } else {
+      if (!wait_warp(&c->xfin, (uint32_t)seg & 1u, c, kSiteXch, j)) return false;
+      l += red_l[r];
+      if (!wait_warp(&c->fin_free, ((uint32_t)seg & 1u) ^ 1u, c, kSiteFinFree, j)) return false;
+      st_cluster_f32(mapa_shared(smem_u32(&c->lfin[r]), partner), l);
+      st_cluster_f32(mapa_shared(smem_u32(&c->mfin[r]), partner), m);
+      mbar_arrive_cluster(&c->fin_full, partner);
+    }
     ++seg;
     return true;
   });
+}
+
+// Score CTAs, one thread: ships each staged P tile and its rescale factors to
+// the value partner with two bulk copies whose bytes complete its p_full.
+__device__ void p_copier(const Params& p, uint8_t* smem, Ctl* c, uint32_t rank, int cluster_id, int n_clusters) {
+  const uint32_t partner = rank + 2;
+  int j = 0;
+  for_items(p, cluster_id, n_clusters, [&](int64_t, const Item& it) {
+    for (int t = it.t0; t < it.t1; ++t, ++j) {
+      const int sb = j & 1;
+      if (!wait(&c->p_staged[sb], (uint32_t)(j >> 1) & 1u, c, kSitePStaged, j)) return false;
+      const uint32_t bar = mapa_shared(smem_u32(&c->p_full[sb]), partner);
+      bulk_copy_s2c(mapa_shared(smem_u32(smem + kOffP + sb * kPBytes), partner), smem + kOffPStage + sb * kPBytes,
+                    kPBytes, bar);
+      bulk_copy_s2c(mapa_shared(smem_u32(&c->alpha[sb][0]), partner), smem + kOffAStage + sb * kRC * 4, kRC * 4, bar);
+      bulk_commit_group();
+    }
+    return true;
+  });
+  bulk_wait_group<0>();  // the copies have landed before this CTA may leave
 }
 
 // ---------------------------------------------------------------------------
 // value pair
 // ---------------------------------------------------------------------------
 __device__ void value_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id, int n_clusters) {
-  // rank 2, whole warp; one elected lane issues each pair MMA
+  // rank 2, whole warp; one elected lane issues each pair MMA, and checks
+  // (without blocking) whether the next tile can start while these run
   const uint32_t tO = c->tmem_base;
   int j = 0;
+  // PV(j) may start once its V tile has landed in both CTAs and P(j) has
+  // landed in both with O holding the rescaled PV(0..j-1)
+  auto ready_test = [&](int jj) {
+    const bool ok = mbar_test_wait_cluster(&c->full[jj % kStagesV], (uint32_t)(jj / kStagesV) & 1u) &&
+                    mbar_test_wait_cluster(&c->o_ready[jj & 1], (uint32_t)(jj >> 1) & 1u);
+    return __all_sync(0xffffffffu, ok);
+  };
   for_items(p, cluster_id, n_clusters, [&](int64_t, const Item& it) {
+    bool ready = false;
     for (int t = it.t0; t < it.t1; ++t, ++j) {
-      const int s = j % kStages, pb = j & 1;
-      const uint32_t ph = (uint32_t)(j / kStages) & 1u;
-      if (!wait_warp(&c->full[s], ph, c, kSiteFullV, j)) return false;
-      if (!wait_warp(&c->full_peer[s], ph, c, kSitePeer, j)) return false;
-      // P(j) landed in both CTAs and O holds the rescaled PV(0..j-1)
-      if (!wait_warp(&c->o_ready[pb], (uint32_t)(j >> 1) & 1u, c, kSiteOReady, j)) return false;
+      const int s = j % kStagesV, pb = j & 1;
+      if (!ready) {
+        if (!wait_warp(&c->full[s], (uint32_t)(j / kStagesV) & 1u, c, kSiteFullV, j)) return false;
+        if (!wait_warp(&c->o_ready[pb], (uint32_t)(j >> 1) & 1u, c, kSiteOReady, j)) return false;
+      }
       fence_proxy_async_smem();
       tc_fence_after();
       const bool first = (t == it.t0);
@@ -498,6 +570,7 @@ __device__ void value_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id
           mma_pair_ss_warp(tO + nh * 256, da + (uint64_t)((kk * 32) >> 4),
                            dv + (uint64_t)((nh * 2 * kAtomV + kk * 16 * 128) >> 4), kIdescPV, !(first && kk == 0));
         }
+        if (kk == 2) ready = (t + 1 < it.t1) && ready_test(j + 1);
       }
       mma_pair_commit_warp(&c->pv_done[pb], 0xC);
       mma_pair_commit_warp(&c->empty[s], 0xC);
@@ -525,22 +598,25 @@ __device__ void value_release(const Params& p, Ctl* c, uint32_t rank, int cluste
   });
 }
 
-// Row warps of a value CTA: per tile, wait for P, rescale this warp's O rows
-// when a factor differs from 1, and tell the MMA-issuing CTA that O is ready;
-// per item, normalise O and write the outputs (or the split partials).
+// Row warps of a value CTA (warpgroup h takes O columns [256 h, 256 h + 256)):
+// per tile, wait for P, rescale this warp's O rows when a factor differs from
+// 1, and tell the MMA-issuing CTA that O is ready; per item, normalise O and
+// write the outputs (or the split partials).
 __device__ void value_rows(const Params& p, Ctl* c, uint32_t rank, int cluster_id, int n_clusters) {
   const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int wq = warp & 3;
+  const int w = (threadIdx.x >> 5) - kWarpRows;  // 0..7
+  const int wq = w & 3;
+  const int h = w >> 2;
   const int r = wq * 32 + lane;
   const int half = (int)(rank & 1);
-  const uint32_t tO = c->tmem_base + ((uint32_t)(wq * 32) << 16);
+  const int col0 = 256 * h;
+  const uint32_t tO = c->tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)col0;
   const float ln2 = 0.69314718055994530942f;
   int j = 0, seg = 0;
   for_items(p, cluster_id, n_clusters, [&](int64_t item, const Item& it) {
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       const int pb = j & 1;
-      if (warp == kWarpRows && lane == 0) mbar_arrive_expect_tx(&c->p_full[pb], kPTxBytes);
+      if (w == 0 && lane == 0) mbar_arrive_expect_tx(&c->p_full[pb], kPTxBytes);
       if (!wait_warp(&c->p_full[pb], (uint32_t)(j >> 1) & 1u, c, kSitePFull, j)) return false;
       if (t != it.t0) {
         const float a = c->alpha[pb][r];
@@ -550,7 +626,7 @@ __device__ void value_rows(const Params& p, Ctl* c, uint32_t rank, int cluster_i
           tc_fence_after();
           // warp-collective TMEM traffic: every row takes part (factor 1 = unchanged)
 #pragma unroll 1
-          for (int c0 = 0; c0 < kDl; c0 += 32) {
+          for (int c0 = 0; c0 < 256; c0 += 32) {
             uint32_t u[32];
             tmem_ld32_sync(tO + c0, u);
 #pragma unroll
@@ -571,7 +647,7 @@ __device__ void value_rows(const Params& p, Ctl* c, uint32_t rank, int cluster_i
     if (!wait_warp(&c->fin_full, (uint32_t)seg & 1u, c, kSiteFinFull, seg)) return false;
     tc_fence_after();
     const float l = c->lfin[r], m = c->mfin[r];
-    mbar_arrive_cluster_relaxed(&c->fin_free, rank - 2);
+    mbar_arrive_cluster_relaxed(&c->fin_free, rank - 2);  // every row thread, 256 arrivals
     ++seg;
     const int row = it.g * kRG + half * kRC + r;
     const bool live = row < p.rows;  // TMEM loads stay warp-wide; only stores are per row
@@ -581,7 +657,7 @@ __device__ void value_rows(const Params& p, Ctl* c, uint32_t rank, int cluster_i
     if (p.splits == 1) {
       uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDl);
 #pragma unroll 1
-      for (int c0 = 0; c0 < kDl; c0 += 32) {
+      for (int c0 = 0; c0 < 256; c0 += 32) {
         uint32_t u[32];
         __syncwarp();
         tmem_ld32_sync(tO + c0, u);
@@ -593,27 +669,27 @@ __device__ void value_rows(const Params& p, Ctl* c, uint32_t rank, int cluster_i
             o.y = pack_bf16(__uint_as_float(u[8 * v + 2]) * inv, __uint_as_float(u[8 * v + 3]) * inv);
             o.z = pack_bf16(__uint_as_float(u[8 * v + 4]) * inv, __uint_as_float(u[8 * v + 5]) * inv);
             o.w = pack_bf16(__uint_as_float(u[8 * v + 6]) * inv, __uint_as_float(u[8 * v + 7]) * inv);
-            dst[c0 / 8 + v] = o;
+            dst[(col0 + c0) / 8 + v] = o;
           }
         }
       }
-      if (live && p.lse) p.lse[orow] = lse;
+      if (live && p.lse && h == 0) p.lse[orow] = lse;
     } else {
       const int64_t prow = item * kRG + half * kRC + r;
       float4* dst = reinterpret_cast<float4*>(p.part_o + prow * kDl);
 #pragma unroll 1
-      for (int c0 = 0; c0 < kDl; c0 += 32) {
+      for (int c0 = 0; c0 < 256; c0 += 32) {
         uint32_t u[32];
         __syncwarp();
         tmem_ld32_sync(tO + c0, u);
         if (live) {
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            dst[c0 / 4 + v] = make_float4(__uint_as_float(u[4 * v + 0]) * inv, __uint_as_float(u[4 * v + 1]) * inv,
+            dst[(col0 + c0) / 4 + v] = make_float4(__uint_as_float(u[4 * v + 0]) * inv, __uint_as_float(u[4 * v + 1]) * inv,
                                           __uint_as_float(u[4 * v + 2]) * inv, __uint_as_float(u[4 * v + 3]) * inv);
         }
       }
-      if (live) p.part_lse[prow] = lse;
+      if (live && h == 0) p.part_lse[prow] = lse;
     }
     // the next item's first PV overwrites O: its o_ready follows these loads
     tc_fence_before();
@@ -634,29 +710,32 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads,
     return;
   }
   Ctl* c = reinterpret_cast<Ctl*>(smem + kOffCtl);
+  const bool leader = (rank & 1) == 0;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&c->full[s], kProducerThreads);
-      mbar_init(&c->full_peer[s], 1);
+    for (int s = 0; s < kStagesMax; ++s) {
+      mbar_init(&c->full[s], kProducerThreads + (leader ? 1 : 0));
       mbar_init(&c->empty[s], 1);
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(&c->s_full[q], 1);
-      mbar_init(&c->s_free[q], rank == 0 ? 5 : 4);
+      mbar_init(&c->s_free[q], 2 * kRowWarps);
+      mbar_init(&c->xch[q], kRowWarps);
+      mbar_init(&c->p_staged[q], kRowWarps);
       mbar_init(&c->p_free[q], 1);
       mbar_init(&c->p_full[q], 1);
       mbar_init(&c->pv_done[q], 1);
-      mbar_init(&c->o_ready[q], 8);
+      mbar_init(&c->o_ready[q], 2 * kRowWarps);
     }
-    mbar_init(&c->q_ready, 8);
-    mbar_init(&c->fin_free, kRC);
+    mbar_init(&c->q_ready, 2 * kRowWarps);
+    mbar_init(&c->fin_free, kRowThreads);
+    mbar_init(&c->xfin, kRowWarps / 2);
     mbar_init(&c->fin_full, kRC);
     mbar_init(&c->drain, 1);
     c->abort = 0;
     c->abort_site = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpTmem) {
+  if (warp == kWarpAux) {
     tmem_alloc_pair(&c->tmem_base, kTmemCols);
     tmem_relinquish_pair();
   }
@@ -666,19 +745,19 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads,
 
   const int cluster_id = blockIdx.x / kClusterCtas;
   const int n_clusters = gridDim.x / kClusterCtas;
-  const bool score = rank < 2, leader = (rank & 1) == 0;
+  const bool score = rank < 2;
   if (warp < kProducerWarps) {
     producer(p, smem, c, warp, rank, cluster_id, n_clusters);
   } else if (warp == kWarpMma) {
     if (!leader) relay(p, c, rank & 2u, cluster_id, n_clusters);
     else if (score) score_mma(p, smem, c, cluster_id, n_clusters);
     else value_mma(p, smem, c, cluster_id, n_clusters);
-  } else if (warp == kWarpRelease) {
+  } else if (warp == kWarpAux) {
     if ((threadIdx.x & 31) == 0) {
-      if (!score) value_release(p, c, rank, cluster_id, n_clusters);
-      else if (!leader) relay_s_free(p, c, cluster_id, n_clusters);
+      if (score) p_copier(p, smem, c, rank, cluster_id, n_clusters);
+      else value_release(p, c, rank, cluster_id, n_clusters);
     }
-  } else if (warp >= kWarpRows) {
+  } else if (warp >= kWarpRows && warp < kWarpRows + kRowWarps) {
     if (score) score_softmax(p, smem, c, rank, cluster_id, n_clusters);
     else value_rows(p, c, rank, cluster_id, n_clusters);
   }
@@ -693,7 +772,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads,
   __syncthreads();
   tc_fence_after();
   cluster_sync();  // no CTA leaves while a peer may still touch its shared memory
-  if (warp == kWarpTmem) tmem_dealloc_pair(c->tmem_base, kTmemCols);
+  if (warp == kWarpAux) tmem_dealloc_pair(c->tmem_base, kTmemCols);
 }
 
 }  // namespace tc
