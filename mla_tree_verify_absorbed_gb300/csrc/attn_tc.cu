@@ -27,10 +27,11 @@
 //     columns) and runs O += P.V as M=256 MMAs (SS form, N=256 twice,
 //     K=64), each CTA staging half of every kv_c row (V split along N) as
 //     an MN-major operand.
-// So each staged byte serves 256 rows, half the gather of a single-CTA
-// design per row, and the smaller stages leave room for six in flight.
-// P (bf16) and the per-row rescale factors of score CTA c travel from its
-// registers into value CTA 2 + c as st.async stores whose bytes complete that
+// So each CTA reads half of every tile from L2 (the other half reaches its
+// tensor core from the pair peer), and the smaller stages leave room for six
+// in flight.  P (bf16) and the per-row rescale factors of score CTA c are
+// staged in its own shared memory and moved to value CTA 2 + c by one thread
+// with a bulk shared::cta -> shared::cluster copy whose bytes complete that
 // CTA's barrier.  The value CTAs rescale their own O rows when a factor
 // differs from 1 and write the outputs.
 //
@@ -47,9 +48,9 @@
 // Signals between CTAs that hand over no data of the signalling thread (a
 // buffer may be reused, a tile has landed, O is ready) use relaxed remote
 // arrives: the data they guard has already been written and observed (cp.async
-// and st.async completion, tcgen05 wait::ld / wait::st) when they are sent,
-// and a cluster-scope release arrive measured about a microsecond while the
-// thread's earlier remote stores drained.  Only the row statistics handed to
+// and bulk-copy completion, tcgen05 wait::ld / wait::st) when they are sent,
+// and a cluster-scope release arrive measured ~770 cycles per signal, more
+// while the thread's earlier remote stores drained.  Only the row statistics handed to
 // the value CTA (st.shared::cluster data) travel under a release arrive.
 //
 // Every wait is bounded; on timeout the kernel raises an abort flag in all
@@ -124,7 +125,7 @@ struct alignas(16) Ctl {
   uint64_t xch[2];              // score: both halves' partial row maxima of a tile written (8 warp arrivals)
   uint64_t xfin;                // score: half 1's partial row sums of an item written (4 warp arrivals)
   uint64_t p_staged[2];         // score: P and alpha of a tile staged locally (8 warp arrivals)
-  uint64_t p_full[2];           // value: P tile and alpha landed (st.async bytes; armed by a row thread)
+  uint64_t p_full[2];           // value: P tile and alpha landed (bulk-copy bytes; armed by a row thread)
   uint64_t pv_done[2];          // value: PV MMAs of a tile complete
   uint64_t o_ready[2];          // value, rank 2: both CTAs' O ready for the tile's PV (16 warp arrivals)
   uint64_t fin_full;            // value: lfin/mfin written (128 remote arrivals)
