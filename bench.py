@@ -37,8 +37,19 @@ from mla_tree_verify_absorbed_gb300 import inputs as I  # noqa: E402
 METRIC = "verify-attn µs/call & effective KV GB/s (% HBM roofline), H=64, 200k prefix"
 UNIT = "us/call"
 WORKLOAD = "c3"
-WORKLOAD_DESC = ("B=1 H=64 prefix=200000 tree=64 nodes (depth<=8) Dl=512 Dr=64 bf16 "
-                 "page_size=1 slots = seeded permutation of a 262144-slot pool")
+WORKLOAD_DESC = {
+    "c3": ("B=1 H=64 prefix=200000 tree=64 nodes (depth<=8) Dl=512 Dr=64 bf16 "
+           "page_size=1 slots = seeded permutation of a 262144-slot pool"),
+    "c6": ("B=1 H=64 prefix=200000 chain of 4 nodes (linear draft) Dl=512 Dr=64 bf16 "
+           "page_size=1 slots = seeded permutation of a 262144-slot pool"),
+}
+
+
+def workload_desc(name: str, p) -> str:
+    if name in WORKLOAD_DESC:
+        return WORKLOAD_DESC[name]
+    return (f"B={p.B} H={p.H} Q={p.Q} prefix={int(np.max(p.prefix_lens))} {p.dtype} "
+            f"page_size={p.page_size}")
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 KERNELS_PER_CALL = 4  # metadata (2), attention, combine
@@ -252,7 +263,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": us_call, "unit": UNIT, "n_gpus": 0,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": us_call / 1000.0,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": f"{args.workload}: {WORKLOAD_DESC}"},
+        "data": "synthetic", "config": {"workload": f"{args.workload}: {workload_desc(args.workload, p)}"},
         "cpu_baseline": {"value": us_call, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{args.steps} steps x {cores} seeded query rows of "
                                    f"{total_rows}; value = mean time per row x all rows"},
@@ -352,7 +363,7 @@ def run_ours(args):
         "metric": METRIC, "value": us_call, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {WORKLOAD_DESC}", "algo": resolved,
+        "config": {"workload": f"{args.workload}: {workload_desc(args.workload, p)}", "algo": resolved,
                    "num_splits": args.num_splits,
                    "l2": "inputs larger than L2: 230 MB of KV read per call (129 MB L2)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

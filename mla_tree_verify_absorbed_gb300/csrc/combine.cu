@@ -11,62 +11,78 @@
 
 namespace mlav {
 
-constexpr int kCombineThreads = 256;  // one warp per row
+constexpr int kCombineThreads = 256;  // 8 warps; one warp per (row, quarter of the 512 columns)
+constexpr int kQuarters = 4;          // 128 columns per warp: one float4 per lane
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   if (*p.err) return;
   const int lane = threadIdx.x & 31;
   const int64_t gw = (int64_t)blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5);
   const int64_t total_rows = (int64_t)p.B * p.rows;
-  if (gw >= total_rows) return;
-  const int b = (int)(gw / p.rows);
-  const int row = (int)(gw % p.rows);
+  if (gw >= total_rows * kQuarters) return;
+  const int64_t grow = gw / kQuarters;
+  const int quarter = (int)(gw % kQuarters);
+  const int b = (int)(grow / p.rows);
+  const int row = (int)(grow % p.rows);
   const int g = row / p.rg;
   const int64_t T = p.seq_tiles[b];
   const int S = p.splits;
   const int r = row - g * p.rg;
   auto item_of = [&](int k) { return ((int64_t)b * S + k) * p.groups + g; };
   auto nonempty = [&](int k) { return ((int64_t)(k + 1) * T) / S > ((int64_t)k * T) / S; };
+  // pass 1: the lanes read the pieces' lse in parallel; warp max
   float M = -INFINITY;
-  for (int k = 0; k < S; ++k)
+  for (int k = lane; k < S; k += 32)
     if (nonempty(k)) M = fmaxf(M, p.part_lse[item_of(k) * p.rg + r]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  // pass 2: weights exp(lse_k - M) (lane k % 32 holds piece k's), warp sum, and
+  // the weighted sum of the pieces' outputs, four pieces' loads in flight
   float L = 0.f;
-  float4 acc[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != -INFINITY) {
-    for (int k = 0; k < S; ++k) {
-      if (!nonempty(k)) continue;
-      const int64_t prow = item_of(k) * p.rg + r;
-      const float w = __expf(p.part_lse[prow] - M);
-      L += w;
-      const float4* o = reinterpret_cast<const float4*>(p.part_o + prow * kDl);
+    for (int k0 = 0; k0 < S; k0 += 32) {
+      const int k = k0 + lane;
+      const float wk = (k < S && nonempty(k)) ? __expf(p.part_lse[item_of(k) * p.rg + r] - M) : 0.f;
+      float wsum = wk;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 v = o[lane + 32 * q];
-        acc[q].x = fmaf(w, v.x, acc[q].x);
-        acc[q].y = fmaf(w, v.y, acc[q].y);
-        acc[q].z = fmaf(w, v.z, acc[q].z);
-        acc[q].w = fmaf(w, v.w, acc[q].w);
+      for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+      L += wsum;
+      const int n = S - k0 < 32 ? S - k0 : 32;
+#pragma unroll 4
+      for (int q = 0; q < n; ++q) {
+        const float w = __shfl_sync(0xffffffffu, wk, q);
+        if (w != 0.f) {
+          const float4 v = reinterpret_cast<const float4*>(p.part_o + (item_of(k0 + q) * p.rg + r) * kDl)
+              [quarter * 32 + lane];
+          acc.x = fmaf(w, v.x, acc.x);
+          acc.y = fmaf(w, v.y, acc.y);
+          acc.z = fmaf(w, v.z, acc.z);
+          acc.w = fmaf(w, v.w, acc.w);
+        }
       }
     }
   }
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
   const int64_t orow = (int64_t)b * p.rows + row;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int64_t d = 4 * (lane + 32 * k);
-    store_out(p.out, p.dtype, orow * kDl + d + 0, acc[k].x * inv);
-    store_out(p.out, p.dtype, orow * kDl + d + 1, acc[k].y * inv);
-    store_out(p.out, p.dtype, orow * kDl + d + 2, acc[k].z * inv);
-    store_out(p.out, p.dtype, orow * kDl + d + 3, acc[k].w * inv);
+  const int64_t d = (int64_t)4 * (quarter * 32 + lane);
+  if (p.dtype == MLA_BF16) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 w2;
+    w2.x = *reinterpret_cast<uint32_t*>(&lo);
+    w2.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDl + d) = w2;
+  } else {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow * kDl + d) =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   }
-  if (lane == 0 && p.lse) p.lse[orow] = (L > 0.f) ? M + logf(L) : -INFINITY;
+  if (quarter == 0 && lane == 0 && p.lse) p.lse[orow] = (L > 0.f) ? M + logf(L) : -INFINITY;
 }
 
 cudaError_t launch_combine(const Params& p, cudaStream_t stream) {
-  const int64_t total_rows = (int64_t)p.B * p.rows;
-  const int64_t blocks = (total_rows + (kCombineThreads / 32) - 1) / (kCombineThreads / 32);
+  const int64_t warps = (int64_t)p.B * p.rows * kQuarters;
+  const int64_t blocks = (warps + (kCombineThreads / 32) - 1) / (kCombineThreads / 32);
   if (blocks == 0) return cudaSuccess;
   combine_kernel<<<(unsigned)blocks, kCombineThreads, 0, stream>>>(p);
   return cudaGetLastError();

@@ -226,6 +226,9 @@ def make_config(name: str, seed: Optional[int] = None) -> Problem:
               page_size=1 slots in a shared 393,216-slot pool.
     ``c5``    B=32 H=128 prefix 8192, 16-node trees, bf16, page_size=64 with
               pages permuted in a 4,200-page pool.
+    ``c6``    B=1 H=64 prefix 200,000, a 4-node chain (a linear draft), bf16,
+              page_size=1 slots as in c3: 256 query rows, the regime where the
+              KV read, not the products, bounds the call.
     """
     if name == "tiny":
         p = make_problem(name=name, dtype="fp32", B=1, H=16, Q=8, prefix_lens=[256],
@@ -246,12 +249,16 @@ def make_config(name: str, seed: Optional[int] = None) -> Problem:
         p = make_problem(name=name, dtype="bf16", B=32, H=128, Q=16, prefix_lens=[8192] * 32,
                          seed=4 if seed is None else seed, layout="paged", page_size=64,
                          n_pages=4200)
+    elif name == "c6":
+        p = make_problem(name=name, dtype="bf16", B=1, H=64, Q=4, prefix_lens=[200000],
+                         seed=5 if seed is None else seed, layout="scattered", pool_slots=262144,
+                         trees=[[-1, 0, 1, 2]])
     else:
         raise ValueError(f"unknown workload {name!r}")
     return p
 
 
-CONFIG_NAMES = ("tiny", "c2", "c3", "c4", "c5")
+CONFIG_NAMES = ("tiny", "c2", "c3", "c4", "c5", "c6")
 
 
 # ----------------------------------------------------------------------------

@@ -1,0 +1,72 @@
+"""The verify call captured in a CUDA graph (needs a GPU).
+
+The call makes no host synchronisation and no allocation when the caller
+passes the outputs and the workspace, so it can be captured once and replayed
+for every verify step of a decode loop.  A replay must give the same bytes as
+an eager call on the same inputs (same partition, same kernels), and must pick
+up inputs updated in place between replays.
+"""
+import numpy as np
+import pytest
+
+from mla_tree_verify_absorbed_gb300 import api
+from mla_tree_verify_absorbed_gb300 import inputs as I
+from tests import parity as PT
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    api.load()
+
+
+def _problem(seed):
+    return I.make_problem(name="graph", dtype="bf16", B=2, H=64, Q=16, prefix_lens=[900, 2100], seed=seed,
+                          layout="scattered", pool_slots=4096)
+
+
+@pytest.mark.parametrize("algo", ["tc", "simt"])
+def test_graph_replay_matches_eager(algo):
+    p = _problem(51)
+    di = api.device_inputs(p)
+    out0, lse0 = api.verify_attn(di, algo=algo)
+    torch.cuda.synchronize()
+
+    out = torch.empty_like(out0)
+    lse = torch.empty_like(lse0)
+    ws = api.alloc_workspace(api.workspace_size(di, 0, algo=algo))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up outside the capture
+        api.verify_attn(di, out=out, lse=lse, workspace=ws, algo=algo)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        api.verify_attn(di, out=out, lse=lse, workspace=ws, algo=algo)
+    out.zero_()
+    lse.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, out0) and torch.equal(lse, lse0)
+    assert api.check(ws) == 0
+
+    # new queries written into the captured buffers: the replay follows them
+    p2 = _problem(52)
+    di.q_lat.copy_(torch.as_tensor(p2.q_lat.view(np.int16)).view(torch.bfloat16).to(di.q_lat.device)
+                   .reshape(di.q_lat.shape))
+    di.q_pe.copy_(torch.as_tensor(p2.q_pe.view(np.int16)).view(torch.bfloat16).to(di.q_pe.device)
+                  .reshape(di.q_pe.shape))
+    g.replay()
+    torch.cuda.synchronize()
+    p.q_lat, p.q_pe = p2.q_lat, p2.q_pe
+    rows = I.all_rows(p)
+    ro, rl = PT.oracle_rows(p, rows)
+    go, gl = PT.gather_rows(out, lse, rows)
+    PT.assert_close(go, ro, "bf16", f"graph/{algo} out")
+    PT.assert_close(gl, rl, "bf16", f"graph/{algo} lse")

@@ -158,7 +158,7 @@ def test_edge_trees(algo):
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("name,heads,needles", [
     ("c2", 8, False), ("c2", 4, True), ("c3", 2, False), ("c3", 2, True),
-    ("c4", 2, False), ("c5", 2, False),
+    ("c4", 2, False), ("c5", 2, False), ("c6", 8, False), ("c6", 8, True),
 ])
 def test_full_size_sampled(name, heads, needles):
     p = PT.workload(name, needles)
