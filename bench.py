@@ -330,6 +330,9 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, p, di, dev, stream, algo, dist)
+    graph = None
+    if not args.no_graph:
+        graph = run_graph(args, p, di, dev, stream, algo, dist)
 
     if rank != 0:
         return 0
@@ -378,10 +381,48 @@ def run_ours(args):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if graph is not None:
+        line["graph"] = graph
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p)
     print(json.dumps(line), flush=True)
     return 0
+
+
+def run_graph(args, p, di, dev, stream, algo, dist):
+    """The same call captured once in a CUDA graph and replayed K times
+    (device-resident inputs): what a decode loop that captures its verify
+    step pays per call."""
+    import torch
+    from mla_tree_verify_absorbed_gb300 import api
+
+    out = torch.empty((p.B, p.Q, p.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((p.B, p.Q, p.H), dtype=torch.float32, device=dev)
+    ws = api.alloc_workspace(api.workspace_size(di, args.num_splits, algo), dev)
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        api.verify_attn(di, out=out, lse=lse, num_splits=args.num_splits, algo=algo, workspace=ws)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        api.verify_attn(di, out=out, lse=lse, num_splits=args.num_splits, algo=algo, workspace=ws)
+    for _ in range(max(1, args.warmup)):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(args.steps):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    ms = max_over_ranks(dist, a.elapsed_time(b), device=dev)
+    world = dist.get_world_size() if dist is not None else 1
+    return {"value": ms * 1000.0 / args.steps / world, "unit": UNIT, "note": "CUDA graph replay"}
 
 
 def run_e2e(args, p, di, dev, stream, algo, dist):
@@ -440,6 +481,7 @@ def main(argv=None):
     ap.add_argument("--algo", default="auto", choices=["auto", "simt", "tc"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3  # timing rule: at least three untimed warm-up steps

@@ -168,6 +168,20 @@ mla_status mla_verify_build_meta(const mla_verify_args *args, void *workspace, s
  * MLA_ERR_CUDA); *bits (may be NULL) receives the raw MLA_DEVERR_* bits. */
 mla_status mla_verify_check(const void *workspace, mla_stream_t stream, uint32_t *bits);
 
+/* Failure-detection self-test.  Runs mla_verify_attn's tensor-core path
+ * (bf16 caches; args->algo AUTO or TC; num_splits automatic) with one extra
+ * device wait, at the start of the score MMA role, on a barrier that nothing
+ * completes, bounded by hold_ns (0 < hold_ns <= 1e9).  That wait gives up,
+ * every CTA of its cluster stops issuing work, drains what it issued and
+ * frees its Tensor Memory, and the call completes with MLA_DEVERR_TIMEOUT in
+ * the workspace error word (and the wait site in the second 32-bit word);
+ * out and lse are not written.  The context stays usable: the next call on
+ * the same workspace runs normally.  Returns MLA_ERR_INVALID_ARG for a zero or
+ * larger hold_ns or an empty problem, MLA_ERR_UNSUPPORTED for other dtypes or
+ * algorithms, otherwise as mla_verify_attn. */
+mla_status mla_verify_selftest_timeout(const mla_verify_args *args, void *workspace, size_t ws_bytes,
+                                       uint64_t hold_ns, mla_stream_t stream);
+
 #define MLA_DEVERR_PREFIX 0x1u   /* prefix_lens[b] < 0 */
 #define MLA_DEVERR_INDPTR 0x2u   /* kv_indptr[0] != 0, or a span != prefix_lens[b] + Q */
 #define MLA_DEVERR_SLOT 0x4u     /* resolved slot outside [0, pool_slots) */

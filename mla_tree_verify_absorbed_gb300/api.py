@@ -28,7 +28,8 @@ DEVERR = {
 
 # every symbol include/mla_verify.h declares
 EXPORTS = ("mla_verify_workspace_size", "mla_verify_attn", "mla_verify_attn_noalloc",
-           "mla_verify_build_meta", "mla_verify_check", "mla_status_str", "mla_verify_abi_version")
+           "mla_verify_build_meta", "mla_verify_check", "mla_status_str", "mla_verify_abi_version",
+           "mla_verify_selftest_timeout")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -80,6 +81,9 @@ def load(path: Optional[str] = None):
     lib.mla_verify_build_meta.argtypes = [ctypes.POINTER(MlaVerifyArgs), ctypes.c_void_p, ctypes.c_size_t,
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                           ctypes.c_void_p]
+    lib.mla_verify_selftest_timeout.restype = ctypes.c_int
+    lib.mla_verify_selftest_timeout.argtypes = [ctypes.POINTER(MlaVerifyArgs), ctypes.c_void_p, ctypes.c_size_t,
+                                                ctypes.c_uint64, ctypes.c_void_p]
     lib.mla_verify_check.restype = ctypes.c_int
     lib.mla_verify_check.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
     lib.mla_status_str.restype = ctypes.c_char_p
@@ -242,6 +246,17 @@ def verify_attn_noalloc(di: DeviceInputs, out=None, lse=None, num_splits: int = 
     if st != MLA_OK:
         raise MlaError(st, "mla_verify_attn_noalloc")
     return out, lse
+
+
+def selftest_timeout(di: DeviceInputs, out, lse, workspace, hold_ns: int, stream=None):
+    """Run mla_verify_selftest_timeout: the tensor-core call with one device
+    wait that gives up after hold_ns; read the outcome with check()."""
+    a = make_args(di, out, lse, "tc")
+    st = load().mla_verify_selftest_timeout(ctypes.byref(a), ctypes.c_void_p(_ptr(workspace)),
+                                            ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                                            ctypes.c_uint64(int(hold_ns)), _stream(stream))
+    if st != MLA_OK:
+        raise MlaError(st, "mla_verify_selftest_timeout")
 
 
 def build_meta(di: DeviceInputs, workspace=None, stream=None):

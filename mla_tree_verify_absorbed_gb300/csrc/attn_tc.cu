@@ -130,6 +130,7 @@ struct alignas(16) Ctl {
   uint64_t o_ready[2];          // value, rank 2: both CTAs' O ready for the tile's PV (16 warp arrivals)
   uint64_t fin_full;            // value: lfin/mfin written (128 remote arrivals)
   uint64_t drain;               // even CTAs: final MMA drain on abort
+  uint64_t hold;                // self-test: never completed
   alignas(16) float alpha[2][kRC];  // value: per-row rescale of O before PV(j) (1 = unchanged; bulk-copy target)
   float lfin[kRC];              // value: final row sums of the weights
   float mfin[kRC];              // value: final running max (base-2 units)
@@ -150,14 +151,17 @@ static_assert(kWarpAux < kThreads / 32, "warp roles exceed the CTA");
 enum {
   kSiteEmpty = 1, kSiteQReady, kSiteFullS, kSiteSFree, kSiteSFull, kSitePFree, kSiteFinFree,
   kSiteFullV, kSiteOReady, kSitePFull, kSitePvPrev, kSitePvLast, kSiteRelease, kSiteRelay, kSiteFinFull,
-  kSiteXch, kSitePStaged
+  kSiteXch, kSitePStaged, kSiteHold
 };
 
 // Bounded wait on a barrier of this CTA.  Barriers that other CTAs (or pair
-// MMA commits) arrive on are waited with cluster-scope acquire.  On giving
-// up, the first site is recorded and every CTA of the cluster is told to stop.
+// MMA commits) arrive on are waited with cluster-scope acquire.  A wait that
+// runs out of time records its site (waits that only see the abort flag
+// record nothing) and tells every CTA of the cluster to stop.
 __device__ __noinline__ void raise_abort(Ctl* c, int site, int j) {
-  atomicCAS(&c->abort_site, 0, (site & 0xff) | ((j & 0xffff) << 16));
+  // a wait that gave up while no abort was raised ran out of time itself
+  if (*reinterpret_cast<volatile int*>(&c->abort) == 0)
+    atomicCAS(&c->abort_site, 0, (site & 0xff) | ((j & 0xffff) << 16));
   for (uint32_t rk = 0; rk < kClusterCtas; ++rk) st_cluster_u32(mapa_shared(smem_u32(&c->abort), rk), 1u);
 }
 __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, Ctl* c, int site, int j,
@@ -317,6 +321,12 @@ __device__ void score_mma(const Params& p, uint8_t* smem, Ctl* c, int cluster_id
   // loaded S(j-2) from buffer j & 1 (the softmax loading S(j-1) from the other
   // buffer meanwhile does not delay these MMAs: measured, a TMEM load of other
   // columns completes in tens of cycles while MMAs run)
+  if (p.hold_ns) {
+    // failure-detection self-test: a wait that nothing completes, bounded by
+    // hold_ns; giving up raises the abort in every CTA of the cluster
+    if (!mbar_wait(&c->hold, 0u, &c->abort, p.hold_ns, true)) raise_abort(c, kSiteHold, 0);
+    __syncwarp();
+  }
   auto ready_test = [&](int jj) {
     const bool ok = mbar_test_wait_cluster(&c->full[jj % kStagesS], (uint32_t)(jj / kStagesS) & 1u) &&
                     (jj < 2 || mbar_test_wait_cluster(&c->s_free[jj & 1], (((uint32_t)jj >> 1) & 1u) ^ 1u));
@@ -732,6 +742,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads,
     mbar_init(&c->xfin, kRowWarps / 2);
     mbar_init(&c->fin_full, kRC);
     mbar_init(&c->drain, 1);
+    mbar_init(&c->hold, 1);
     c->abort = 0;
     c->abort_site = 0;
     fence_mbar_init();

@@ -211,8 +211,11 @@ size_t mla_verify_workspace_size(const mla_verify_args* a, int num_splits) {
   return pl.L.total;
 }
 
-mla_status mla_verify_attn(const mla_verify_args* a, void* workspace, size_t ws_bytes, int num_splits,
-                           mla_stream_t stream) {
+}  // extern "C"
+
+namespace {
+mla_status run_attn(const mla_verify_args* a, void* workspace, size_t ws_bytes, int num_splits,
+                    mla_stream_t stream, uint64_t hold_ns) {
   Plan pl;
   mla_status st = make_plan(a, num_splits, &pl);
   if (st != MLA_OK) return st;
@@ -228,7 +231,8 @@ mla_status mla_verify_attn(const mla_verify_args* a, void* workspace, size_t ws_
     pl.grid = (int)(pl.items < cap ? pl.items : cap);
     if (pl.grid < 1) pl.grid = 1;
   }
-  const Params p = make_params(a, pl, workspace);
+  Params p = make_params(a, pl, workspace);
+  p.hold_ns = hold_ns;
   if (launch_meta(p, pl.sm_count, nullptr, 0, nullptr, s) != cudaSuccess) return MLA_ERR_CUDA;
   if (a->profile_events && cudaEventRecord((cudaEvent_t)a->profile_events[0], s) != cudaSuccess)
     return MLA_ERR_CUDA;
@@ -238,6 +242,25 @@ mla_status mla_verify_attn(const mla_verify_args* a, void* workspace, size_t ws_
     return MLA_ERR_CUDA;
   if (pl.splits > 1 && launch_combine(p, s) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+mla_status mla_verify_attn(const mla_verify_args* a, void* workspace, size_t ws_bytes, int num_splits,
+                           mla_stream_t stream) {
+  return run_attn(a, workspace, ws_bytes, num_splits, stream, 0);
+}
+
+mla_status mla_verify_selftest_timeout(const mla_verify_args* a, void* workspace, size_t ws_bytes,
+                                       uint64_t hold_ns, mla_stream_t stream) {
+  if (!a) return MLA_ERR_INVALID_ARG;
+  if (hold_ns == 0 || hold_ns > 1000000000ull) return MLA_ERR_INVALID_ARG;
+  if (a->dtype != MLA_BF16 || (a->algo != MLA_ALGO_AUTO && a->algo != MLA_ALGO_TC)) return MLA_ERR_UNSUPPORTED;
+  mla_verify_args t = *a;
+  t.algo = MLA_ALGO_TC;
+  if (t.B == 0 || t.Q == 0) return MLA_ERR_INVALID_ARG;  // the self-test needs a launch
+  return run_attn(&t, workspace, ws_bytes, 0, stream, hold_ns);
 }
 
 mla_status mla_verify_build_meta(const mla_verify_args* a, void* workspace, size_t ws_bytes, uint64_t* anc,

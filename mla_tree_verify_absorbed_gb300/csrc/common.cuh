@@ -55,6 +55,10 @@ struct Params {
   int64_t* seq_kv_base;    // [B+1] cumulative N_b
   float* part_lse;         // [n_items][rg]  (natural log)
   float* part_o;           // [n_items][rg][512], normalised partial outputs
+
+  // failure-detection self-test only (0 otherwise): the tensor-core kernel
+  // first waits, at most this many ns, on a barrier nothing completes
+  uint64_t hold_ns;
 };
 
 // ---------------------------------------------------------------------------

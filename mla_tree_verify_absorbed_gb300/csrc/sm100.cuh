@@ -101,8 +101,8 @@ __device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t p
   return ok != 0;
 }
 
-// Bounded wait: spins until the phase with `parity` completes or `abort` is
-// raised or `limit_ns` passes; on timeout sets *abort and returns false.
+// Bounded wait: true once the phase with `parity` completes; false when
+// `abort` is raised or `limit_ns` passes first (the caller raises the abort).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns, bool cluster_scope = false) {
   if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
@@ -110,10 +110,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   while (true) {
     if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > limit_ns) {
-      *abort = 1;
-      return false;
-    }
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

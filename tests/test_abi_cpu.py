@@ -138,3 +138,16 @@ def test_build_meta_validation(lib):
     st = lib.mla_verify_build_meta(ctypes.byref(a), ctypes.c_void_p(0x100000), ctypes.c_size_t(1 << 40),
                                    None, ctypes.c_void_p(0x200000), ctypes.c_int64(10), None)
     assert st == api.MLA_ERR_INVALID_ARG
+
+
+def test_selftest_timeout_argument_checks(lib):
+    # rejected on the host, before any device call
+    a = fake_args()
+    ws = ctypes.c_void_p(0x100000)
+    assert lib.mla_verify_selftest_timeout(ctypes.byref(a), ws, 1 << 20, 0, None) == api.MLA_ERR_INVALID_ARG
+    assert lib.mla_verify_selftest_timeout(ctypes.byref(a), ws, 1 << 20, 2_000_000_000, None) == \
+        api.MLA_ERR_INVALID_ARG
+    f = fake_args(dtype=api.MLA_FP32)
+    assert lib.mla_verify_selftest_timeout(ctypes.byref(f), ws, 1 << 20, 1000, None) == api.MLA_ERR_UNSUPPORTED
+    s = fake_args(algo=api.ALGO["simt"])
+    assert lib.mla_verify_selftest_timeout(ctypes.byref(s), ws, 1 << 20, 1000, None) == api.MLA_ERR_UNSUPPORTED
