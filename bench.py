@@ -333,6 +333,9 @@ def run_ours(args):
     graph = None
     if not args.no_graph:
         graph = run_graph(args, p, di, dev, stream, algo, dist)
+    compact = None
+    if args.compact:
+        compact = run_compact(args, p, di, dev, stream, dist)
 
     if rank != 0:
         return 0
@@ -383,10 +386,61 @@ def run_ours(args):
         line["e2e"] = e2e
     if graph is not None:
         line["graph"] = graph
+    if compact is not None:
+        line["kv_compact"] = compact
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p)
     print(json.dumps(line), flush=True)
     return 0
+
+
+def run_compact(args, p, di, dev, stream, dist):
+    """KV compaction of the workload's rows into a contiguous destination:
+    us per call and the HBM bandwidth it reaches (each row read once and
+    written once)."""
+    import torch
+    from mla_tree_verify_absorbed_gb300 import api
+
+    total = int(np.sum(np.asarray(p.prefix_lens, dtype=np.int64) + p.Q))
+    dst = torch.empty((total, 576), dtype=torch.bfloat16, device=dev)
+    new_idx = torch.empty((total,), dtype=torch.int32, device=dev)
+    new_indptr = torch.empty((p.B + 1,), dtype=torch.int32, device=dev)
+    ws = api.alloc_workspace(api.workspace_size(di, 1), dev)
+    for _ in range(max(1, args.warmup)):
+        api.kv_compact_into(di, dst, new_idx, new_indptr, ws)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    a.record(stream)
+    for _ in range(args.steps):
+        api.kv_compact_into(di, dst, new_idx, new_indptr, ws)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    if api.check(ws) != 0:
+        raise RuntimeError("kv compaction reported a device error")
+    ms = max_over_ranks(dist, a.elapsed_time(b), device=dev) / args.steps
+    moved = 2.0 * total * 576 * 2
+    hbm_peak, src = peak_hbm_gbs()
+    gbs = moved / (ms / 1000.0) / 1e9
+    # the verify call on the compacted (contiguous) layout
+    import dataclasses
+    dc = dataclasses.replace(di, kv_c=dst[:, :512], k_pe=dst[:, 512:], pool=dst, page_size=1,
+                             kv_indptr=new_indptr, kv_indices=new_idx, block_table=None)
+    out = torch.empty((p.B, p.Q, p.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((p.B, p.Q, p.H), dtype=torch.float32, device=dev)
+    vws = api.alloc_workspace(api.workspace_size(dc, args.num_splits), dev)
+    for _ in range(max(1, args.warmup)):
+        api.verify_attn(dc, out=out, lse=lse, num_splits=args.num_splits, workspace=vws)
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(args.steps):
+        api.verify_attn(dc, out=out, lse=lse, num_splits=args.num_splits, workspace=vws)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    vms = max_over_ranks(dist, a.elapsed_time(b), device=dev) / args.steps
+    return {"us_per_call": ms * 1000.0, "rows": total, "bytes_moved": moved, "gbs": gbs,
+            "hbm_frac": gbs / hbm_peak, "hbm_peak_source": src,
+            "verify_us_on_compacted": vms * 1000.0}
 
 
 def run_graph(args, p, di, dev, stream, algo, dist):
@@ -482,6 +536,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--compact", action="store_true", help="also time KV compaction of the workload's rows")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3  # timing rule: at least three untimed warm-up steps

@@ -168,6 +168,30 @@ mla_status mla_verify_build_meta(const mla_verify_args *args, void *workspace, s
  * MLA_ERR_CUDA); *bits (may be NULL) receives the raw MLA_DEVERR_* bits. */
 mla_status mla_verify_check(const void *workspace, mla_stream_t stream, uint32_t *bits);
 
+/* KV compaction ("Ground Truth in Silicon ...", section "Why This Message Was
+ * Written": KV-cache defragmentation).  For every sequence b and logical
+ * position p in [0, prefix_lens[b] + Q) -- prefix first, then the tree nodes,
+ * the order mla_verify_attn reads them -- copies the kv_c and k_pe rows of the
+ * slot that position resolves to (page_size 1 or paged, as in args) to slot
+ * dst_slot0 + base[b] + p of the destination arrays, where base[b] is the sum
+ * of the earlier sequences' lengths; writes new_kv_indices[base[b] + p] = that
+ * slot and, when new_kv_indptr is not NULL, new_kv_indptr[b] = base[b]
+ * (B + 1 entries).  With those two tables and page_size = 1 the verify call on
+ * the destination gives the same bytes as on the source.
+ *   dst_kv_c, dst_k_pe: device arrays of dst_slots rows, row strides in
+ *     elements (>= 512 / >= 64, multiples of 16 bytes), 16-byte aligned, the
+ *     cache's dtype; they must not overlap any source row;
+ *   dst_slot0 >= 0; dst_slots <= INT32_MAX; rows that would land at or beyond
+ *     dst_slots are skipped and MLA_DEVERR_CAPACITY is recorded;
+ *   workspace as for mla_verify_attn with num_splits = 1; args as for
+ *   mla_verify_attn (queries, outputs and scale are not read).
+ * Device-side table errors are reported as for mla_verify_attn
+ * (mla_verify_check) and then nothing is copied.  Asynchronous on `stream`. */
+mla_status mla_kv_compact(const mla_verify_args *args, void *workspace, size_t ws_bytes, void *dst_kv_c,
+                          void *dst_k_pe, int64_t dst_kv_c_stride, int64_t dst_k_pe_stride, int64_t dst_slot0,
+                          int64_t dst_slots, int32_t *new_kv_indices, int32_t *new_kv_indptr,
+                          mla_stream_t stream);
+
 /* Failure-detection self-test.  Runs mla_verify_attn's tensor-core path
  * (bf16 caches; args->algo AUTO or TC; num_splits automatic) with one extra
  * device wait, at the start of the score MMA role, on a barrier that nothing

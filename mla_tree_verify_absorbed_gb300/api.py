@@ -29,7 +29,7 @@ DEVERR = {
 # every symbol include/mla_verify.h declares
 EXPORTS = ("mla_verify_workspace_size", "mla_verify_attn", "mla_verify_attn_noalloc",
            "mla_verify_build_meta", "mla_verify_check", "mla_status_str", "mla_verify_abi_version",
-           "mla_verify_selftest_timeout")
+           "mla_verify_selftest_timeout", "mla_kv_compact")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -84,6 +84,10 @@ def load(path: Optional[str] = None):
     lib.mla_verify_selftest_timeout.restype = ctypes.c_int
     lib.mla_verify_selftest_timeout.argtypes = [ctypes.POINTER(MlaVerifyArgs), ctypes.c_void_p, ctypes.c_size_t,
                                                 ctypes.c_uint64, ctypes.c_void_p]
+    lib.mla_kv_compact.restype = ctypes.c_int
+    lib.mla_kv_compact.argtypes = [ctypes.POINTER(MlaVerifyArgs), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                   ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     lib.mla_verify_check.restype = ctypes.c_int
     lib.mla_verify_check.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
     lib.mla_status_str.restype = ctypes.c_char_p
@@ -257,6 +261,38 @@ def selftest_timeout(di: DeviceInputs, out, lse, workspace, hold_ns: int, stream
                                             ctypes.c_uint64(int(hold_ns)), _stream(stream))
     if st != MLA_OK:
         raise MlaError(st, "mla_verify_selftest_timeout")
+
+
+def kv_compact(di: DeviceInputs, dst_pool, dst_slot0: int = 0, workspace=None, stream=None):
+    """Run mla_kv_compact into ``dst_pool`` ([slots][576] of the cache dtype:
+    kv_c columns 0-511, k_pe 512-575); returns (new_kv_indices [sum N_b] int32,
+    new_kv_indptr [B+1] int32, workspace)."""
+    import torch
+    dev = di.q_lat.device
+    a = make_args(di)
+    lib = load()
+    need = lib.mla_verify_workspace_size(ctypes.byref(a), 1)
+    if workspace is None:
+        workspace = alloc_workspace(need, dev)
+    total = int((di.prefix_lens.to(torch.int64) + di.Q).sum().item())
+    new_idx = torch.full((max(total, 1),), -1, dtype=torch.int32, device=dev)
+    new_indptr = torch.zeros((di.B + 1,), dtype=torch.int32, device=dev)
+    kv_compact_into(di, dst_pool, new_idx, new_indptr, workspace, dst_slot0, stream)
+    return new_idx[:total], new_indptr, workspace
+
+
+def kv_compact_into(di: DeviceInputs, dst_pool, new_idx, new_indptr, workspace, dst_slot0: int = 0, stream=None):
+    """mla_kv_compact with caller-provided output tables (no host synchronisation)."""
+    a = make_args(di)
+    lib = load()
+    st = lib.mla_kv_compact(ctypes.byref(a), ctypes.c_void_p(_ptr(workspace)),
+                            ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                            ctypes.c_void_p(_ptr(dst_pool)), ctypes.c_void_p(_ptr(dst_pool[:, 512:])),
+                            ctypes.c_int64(dst_pool.stride(0)), ctypes.c_int64(dst_pool.stride(0)),
+                            ctypes.c_int64(dst_slot0), ctypes.c_int64(dst_pool.shape[0]),
+                            ctypes.c_void_p(_ptr(new_idx)), ctypes.c_void_p(_ptr(new_indptr)), _stream(stream))
+    if st != MLA_OK:
+        raise MlaError(st, "mla_kv_compact")
 
 
 def build_meta(di: DeviceInputs, workspace=None, stream=None):

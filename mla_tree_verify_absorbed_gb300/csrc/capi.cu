@@ -21,6 +21,9 @@ int tc_tokens_per_tile();
 int tc_clusters_per_gpu(int sm_count);
 int simt_ctas_per_gpu(int sm_count);
 int tc_default_for(int dtype);
+cudaError_t launch_compact(const Params& p, int sm_count, void* dst_kvc, void* dst_kpe, int64_t dkvc_stride,
+                           int64_t dkpe_stride, int64_t dst_slot0, int64_t dst_slots, int32_t* new_idx,
+                           int32_t* new_indptr, cudaStream_t stream);
 }  // namespace mlav
 
 using namespace mlav;
@@ -261,6 +264,38 @@ mla_status mla_verify_selftest_timeout(const mla_verify_args* a, void* workspace
   t.algo = MLA_ALGO_TC;
   if (t.B == 0 || t.Q == 0) return MLA_ERR_INVALID_ARG;  // the self-test needs a launch
   return run_attn(&t, workspace, ws_bytes, 0, stream, hold_ns);
+}
+
+mla_status mla_kv_compact(const mla_verify_args* a, void* workspace, size_t ws_bytes, void* dst_kv_c,
+                          void* dst_k_pe, int64_t dst_kv_c_stride, int64_t dst_k_pe_stride, int64_t dst_slot0,
+                          int64_t dst_slots, int32_t* new_kv_indices, int32_t* new_kv_indptr,
+                          mla_stream_t stream) {
+  Plan pl;
+  mla_status st = make_plan(a, 1, &pl);
+  if (st != MLA_OK) return st;
+  st = validate_tables(a);
+  if (st != MLA_OK) return st;
+  if (!dst_kv_c || !dst_k_pe || !new_kv_indices) return MLA_ERR_INVALID_ARG;
+  const int64_t el = a->dtype == MLA_BF16 ? 2 : 4;
+  if (!aligned16(dst_kv_c) || !aligned16(dst_k_pe)) return MLA_ERR_INVALID_ARG;
+  // source rows are read with 16-byte vector loads too
+  if (!a->kv_c || !a->k_pe || !aligned16(a->kv_c) || !aligned16(a->k_pe) || (a->kv_c_stride * el) % 16 ||
+      (a->k_pe_stride * el) % 16)
+    return MLA_ERR_INVALID_ARG;
+  if (dst_kv_c_stride < 512 || dst_k_pe_stride < 64 || (dst_kv_c_stride * el) % 16 || (dst_k_pe_stride * el) % 16)
+    return MLA_ERR_INVALID_ARG;
+  if (dst_slot0 < 0 || dst_slots < 0 || dst_slots > INT32_MAX) return MLA_ERR_INVALID_ARG;
+  if (pl.noop) return MLA_OK;
+  st = check_ws(pl, workspace, ws_bytes);
+  if (st != MLA_OK) return st;
+  if (device_sm_count(&pl.sm_count) != 0) return MLA_ERR_CUDA;
+  const Params p = make_params(a, pl, workspace);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_meta(p, pl.sm_count, nullptr, 0, nullptr, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_compact(p, pl.sm_count, dst_kv_c, dst_k_pe, dst_kv_c_stride, dst_k_pe_stride, dst_slot0, dst_slots,
+                     new_kv_indices, new_kv_indptr, s) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
 }
 
 mla_status mla_verify_build_meta(const mla_verify_args* a, void* workspace, size_t ws_bytes, uint64_t* anc,

@@ -151,3 +151,22 @@ def test_selftest_timeout_argument_checks(lib):
     assert lib.mla_verify_selftest_timeout(ctypes.byref(f), ws, 1 << 20, 1000, None) == api.MLA_ERR_UNSUPPORTED
     s = fake_args(algo=api.ALGO["simt"])
     assert lib.mla_verify_selftest_timeout(ctypes.byref(s), ws, 1 << 20, 1000, None) == api.MLA_ERR_UNSUPPORTED
+
+
+def test_kv_compact_argument_checks(lib):
+    a = fake_args()
+    ws = ctypes.c_void_p(0x100000)
+    good = dict(dst_kv_c=0x200000, dst_k_pe=0x200400, s1=576, s2=576, slot0=0, slots=1 << 20, idx=0x300000)
+
+    def call(**kw):
+        c = dict(good, **kw)
+        return lib.mla_kv_compact(ctypes.byref(a), ws, 1 << 24, c["dst_kv_c"], c["dst_k_pe"], c["s1"], c["s2"],
+                                  c["slot0"], c["slots"], c["idx"], None, None)
+    assert call(dst_kv_c=None) == api.MLA_ERR_INVALID_ARG
+    assert call(idx=None) == api.MLA_ERR_INVALID_ARG
+    assert call(dst_k_pe=0x200408) == api.MLA_ERR_INVALID_ARG   # not 16-byte aligned
+    assert call(s1=500) == api.MLA_ERR_INVALID_ARG              # a destination row must hold 512 elements
+    assert call(s2=60) == api.MLA_ERR_INVALID_ARG
+    assert call(s1=577) == api.MLA_ERR_INVALID_ARG              # row stride not a multiple of 16 bytes
+    assert call(slot0=-1) == api.MLA_ERR_INVALID_ARG
+    assert call(slots=1 << 40) == api.MLA_ERR_INVALID_ARG
