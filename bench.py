@@ -336,6 +336,9 @@ def run_ours(args):
     compact = None
     if args.compact:
         compact = run_compact(args, p, di, dev, stream, dist)
+    ddtree = None
+    if not args.no_ddtree:
+        ddtree = run_ddtree(args, dev, stream, dist, with_oracle=(world == 1 and not args.no_cpu_baseline))
 
     if rank != 0:
         return 0
@@ -388,6 +391,8 @@ def run_ours(args):
         line["graph"] = graph
     if compact is not None:
         line["kv_compact"] = compact
+    if ddtree is not None:
+        line["ddtree"] = ddtree
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p)
     print(json.dumps(line), flush=True)
@@ -441,6 +446,67 @@ def run_compact(args, p, di, dev, stream, dist):
     return {"us_per_call": ms * 1000.0, "rows": total, "bytes_moved": moved, "gbs": gbs,
             "hbm_frac": gbs / hbm_peak, "hbm_peak_source": src,
             "verify_us_on_compacted": vms * 1000.0}
+
+
+def run_ddtree(args, dev, stream, dist, with_oracle: bool):
+    """DDTree construction and greedy acceptance around the verify call: us per
+    call at one sequence (the 64-node tree of the verify workload) and at 256
+    sequences.  Both kernels are latency-bound (one warp per sequence, a chain
+    of `budget` dependent selection steps), so the figure of merit is the
+    per-call latency and the cycles per selection step."""
+    import torch
+    from mla_tree_verify_absorbed_gb300 import api
+    from mla_tree_verify_absorbed_gb300 import draft_inputs as DI
+
+    res = {}
+    steps = max(20, args.steps)
+    for name in ("tree_b1", "tree_b256"):
+        d = DI.make_draft_config(name)
+        root = torch.from_numpy(d.root_token).to(dev)
+        ctok = torch.from_numpy(d.cand_token).to(dev)
+        clp = torch.from_numpy(d.cand_logp).to(dev)
+        i32 = dict(dtype=torch.int32, device=dev)
+        parent, token = torch.empty((d.B, d.Q), **i32), torch.empty((d.B, d.Q), **i32)
+        ws = api.alloc_workspace(api.DDTREE_WORKSPACE_BYTES, dev)
+        api.ddtree_build_into(root, ctok, clp, d.budget, parent, token, ws)
+        torch.cuda.synchronize(dev)
+        tgt = torch.from_numpy(DI.make_targets(d, parent.cpu().numpy(), seed=5, p_follow=0.8)).to(dev)
+        n_len, nodes, nxt = torch.empty((d.B,), **i32), torch.empty((d.B, d.Q), **i32), torch.empty((d.B,), **i32)
+        ws_a = api.alloc_workspace(api.DDTREE_WORKSPACE_BYTES, dev)
+
+        def timed(fn):
+            for _ in range(max(3, args.warmup)):
+                fn()
+            torch.cuda.synchronize(dev)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            barrier(dist)
+            a.record(stream)
+            for _ in range(steps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            return max_over_ranks(dist, a.elapsed_time(b), device=dev) * 1000.0 / steps
+
+        build_us = timed(lambda: api.ddtree_build_into(root, ctok, clp, d.budget, parent, token, ws))
+        accept_us = timed(lambda: api.ddtree_accept_into(parent, token, tgt, n_len, nodes, nxt, ws_a))
+        if api.check(ws) or api.check(ws_a):
+            raise RuntimeError("ddtree kernels reported a device error")
+        # both calls replayed from one CUDA graph (a decode step's launch pattern)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            api.ddtree_build_into(root, ctok, clp, d.budget, parent, token, ws)
+            api.ddtree_accept_into(parent, token, tgt, n_len, nodes, nxt, ws_a)
+        graph_us = timed(g.replay)
+        entry = {"B": d.B, "L": d.L, "K": d.K, "budget": d.budget, "build_us": build_us,
+                 "accept_us": accept_us, "build_plus_accept_graph_us": graph_us,
+                 "mean_accept_len": float(n_len.float().mean().item())}
+        if with_oracle:
+            t0 = time.perf_counter()
+            from oracle import ddtree as odd  # CPU baseline leg only
+            odd.build_tree(d.root_token, d.cand_token, d.cand_logp, d.budget)
+            entry["cpu_baseline_build_us"] = (time.perf_counter() - t0) * 1e6
+        res[name] = entry
+    return res
 
 
 def run_graph(args, p, di, dev, stream, algo, dist):
@@ -537,6 +603,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--compact", action="store_true", help="also time KV compaction of the workload's rows")
+    ap.add_argument("--no-ddtree", action="store_true", help="skip the DDTree construction / acceptance timing")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3  # timing rule: at least three untimed warm-up steps

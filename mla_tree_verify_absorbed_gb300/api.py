@@ -1,4 +1,4 @@
-"""ctypes binding of the C ABI in include/mla_verify.h.
+"""ctypes binding of the C ABI in include/mla_verify.h and include/mla_ddtree.h.
 
 Argument marshalling only: torch tensors give device pointers, sizes and
 strides; every step of the computation runs in the CUDA library.  The library
@@ -23,14 +23,15 @@ ALGO = {"auto": 0, "simt": 1, "tc": 2}
 
 DEVERR = {
     0x1: "PREFIX", 0x2: "INDPTR", 0x4: "SLOT", 0x8: "PARENT", 0x10: "PAGES",
-    0x20: "CAPACITY", 0x40: "TIMEOUT", 0x80: "LAYOUT",
+    0x20: "CAPACITY", 0x40: "TIMEOUT", 0x80: "LAYOUT", 0x100: "DRAFT",
 }
 
-# every symbol include/mla_verify.h declares
+# every symbol include/*.h declares
 EXPORTS = ("mla_verify_workspace_size", "mla_verify_attn", "mla_verify_attn_noalloc",
            "mla_verify_build_meta", "mla_verify_check", "mla_status_str", "mla_verify_abi_version",
-           "mla_verify_selftest_timeout", "mla_kv_compact")
+           "mla_verify_selftest_timeout", "mla_kv_compact", "mla_ddtree_build", "mla_ddtree_accept")
 NOALLOC_SCRATCH_BYTES = 32 << 20
+DDTREE_WORKSPACE_BYTES = 256
 
 
 class MlaVerifyArgs(ctypes.Structure):
@@ -49,6 +50,25 @@ class MlaVerifyArgs(ctypes.Structure):
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
         ("algo", ctypes.c_int),
         ("profile_events", ctypes.c_void_p),
+    ]
+
+
+class MlaDdtreeBuildArgs(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int), ("L", ctypes.c_int), ("K", ctypes.c_int), ("budget", ctypes.c_int),
+        ("root_token", ctypes.c_void_p), ("cand_token", ctypes.c_void_p), ("cand_logp", ctypes.c_void_p),
+        ("tree_parent", ctypes.c_void_p), ("tree_token", ctypes.c_void_p),
+        ("tree_depth", ctypes.c_void_p), ("tree_score", ctypes.c_void_p),
+    ]
+
+
+class MlaDdtreeAcceptArgs(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int), ("Q", ctypes.c_int),
+        ("tree_parent", ctypes.c_void_p), ("tree_token", ctypes.c_void_p), ("target_token", ctypes.c_void_p),
+        ("node_slot", ctypes.c_void_p),
+        ("accept_len", ctypes.c_void_p), ("accept_nodes", ctypes.c_void_p), ("accept_slots", ctypes.c_void_p),
+        ("next_token", ctypes.c_void_p),
     ]
 
 
@@ -88,6 +108,12 @@ def load(path: Optional[str] = None):
     lib.mla_kv_compact.argtypes = [ctypes.POINTER(MlaVerifyArgs), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                    ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    lib.mla_ddtree_build.restype = ctypes.c_int
+    lib.mla_ddtree_build.argtypes = [ctypes.POINTER(MlaDdtreeBuildArgs), ctypes.c_void_p, ctypes.c_size_t,
+                                     ctypes.c_void_p]
+    lib.mla_ddtree_accept.restype = ctypes.c_int
+    lib.mla_ddtree_accept.argtypes = [ctypes.POINTER(MlaDdtreeAcceptArgs), ctypes.c_void_p, ctypes.c_size_t,
+                                      ctypes.c_void_p]
     lib.mla_verify_check.restype = ctypes.c_int
     lib.mla_verify_check.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
     lib.mla_status_str.restype = ctypes.c_char_p
@@ -322,3 +348,74 @@ def check(workspace, stream=None) -> int:
     if st not in (MLA_OK, MLA_ERR_DEVICE_CHECK):
         raise MlaError(st, "mla_verify_check")
     return int(bits.value)
+
+
+# ----------------------------------------------------------------------------
+# DDTree construction and acceptance (include/mla_ddtree.h)
+# ----------------------------------------------------------------------------
+def _ws_bytes(workspace) -> int:
+    return workspace.numel() * workspace.element_size()
+
+
+def ddtree_build_into(root_token, cand_token, cand_logp, budget: int, tree_parent, tree_token, workspace,
+                      tree_depth=None, tree_score=None, stream=None):
+    """mla_ddtree_build into caller-provided [B][budget+1] outputs (no host synchronisation)."""
+    B, L, K = cand_logp.shape
+    a = MlaDdtreeBuildArgs()
+    a.B, a.L, a.K, a.budget = B, L, K, int(budget)
+    a.root_token, a.cand_token, a.cand_logp = _ptr(root_token), _ptr(cand_token), _ptr(cand_logp)
+    a.tree_parent, a.tree_token = _ptr(tree_parent), _ptr(tree_token)
+    a.tree_depth, a.tree_score = _ptr(tree_depth), _ptr(tree_score)
+    st = load().mla_ddtree_build(ctypes.byref(a), ctypes.c_void_p(_ptr(workspace)),
+                                 ctypes.c_size_t(_ws_bytes(workspace)), _stream(stream))
+    if st != MLA_OK:
+        raise MlaError(st, "mla_ddtree_build")
+
+
+def ddtree_build(root_token, cand_token, cand_logp, budget: int, workspace=None, stream=None):
+    """Build the draft trees; inputs are device tensors [B] int32, [B][L][K] int32,
+    [B][L][K] float32.  Returns (parent, token, depth, score) [B][budget+1] and the workspace."""
+    import torch
+    dev = cand_logp.device
+    B = cand_logp.shape[0]
+    Q = int(budget) + 1
+    if workspace is None:
+        workspace = alloc_workspace(DDTREE_WORKSPACE_BYTES, dev)
+    parent = torch.full((B, Q), -7, dtype=torch.int32, device=dev)
+    token = torch.full((B, Q), -7, dtype=torch.int32, device=dev)
+    depth = torch.full((B, Q), -7, dtype=torch.int32, device=dev)
+    score = torch.full((B, Q), float("nan"), dtype=torch.float32, device=dev)
+    ddtree_build_into(root_token, cand_token, cand_logp, budget, parent, token, workspace, depth, score, stream)
+    return parent, token, depth, score, workspace
+
+
+def ddtree_accept_into(tree_parent, tree_token, target_token, accept_len, accept_nodes, next_token, workspace,
+                       node_slot=None, accept_slots=None, stream=None):
+    """mla_ddtree_accept into caller-provided outputs (no host synchronisation)."""
+    B, Q = tree_parent.shape
+    a = MlaDdtreeAcceptArgs()
+    a.B, a.Q = B, Q
+    a.tree_parent, a.tree_token, a.target_token = _ptr(tree_parent), _ptr(tree_token), _ptr(target_token)
+    a.node_slot = _ptr(node_slot)
+    a.accept_len, a.accept_nodes, a.accept_slots = _ptr(accept_len), _ptr(accept_nodes), _ptr(accept_slots)
+    a.next_token = _ptr(next_token)
+    st = load().mla_ddtree_accept(ctypes.byref(a), ctypes.c_void_p(_ptr(workspace)),
+                                  ctypes.c_size_t(_ws_bytes(workspace)), _stream(stream))
+    if st != MLA_OK:
+        raise MlaError(st, "mla_ddtree_accept")
+
+
+def ddtree_accept(tree_parent, tree_token, target_token, node_slot=None, workspace=None, stream=None):
+    """Greedy acceptance; inputs are device int32 tensors [B][Q].  Returns
+    (accept_len [B], accept_nodes [B][Q], next_token [B], accept_slots [B][Q] or None, workspace)."""
+    import torch
+    dev = tree_parent.device
+    B, Q = tree_parent.shape
+    if workspace is None:
+        workspace = alloc_workspace(DDTREE_WORKSPACE_BYTES, dev)
+    n_len = torch.full((B,), -7, dtype=torch.int32, device=dev)
+    nodes = torch.full((B, Q), -7, dtype=torch.int32, device=dev)
+    nxt = torch.full((B,), -7, dtype=torch.int32, device=dev)
+    slots = None if node_slot is None else torch.full((B, Q), -7, dtype=torch.int32, device=dev)
+    ddtree_accept_into(tree_parent, tree_token, target_token, n_len, nodes, nxt, workspace, node_slot, slots, stream)
+    return n_len, nodes, nxt, slots, workspace

@@ -1,0 +1,359 @@
+// DDTree draft-tree construction and greedy token acceptance, with their C
+// ABI (include/mla_ddtree.h).
+//
+// The pages name both steps as kernels of the DFlash / DDTree project next to
+// tree-verify attention ("Reading the Reference: How a Single File-Read
+// Message Anchored a Complex CUDA Kernel Implementation", section "Input
+// Knowledge Required to Understand This Message", item 1); the rules
+// implemented are the readings stated in the header.
+//
+// Both are latency-bound: a sequence is a few hundred bytes of input and its
+// selection is a chain of `budget` dependent steps, so each sequence gets one
+// warp and the whole working set lives in registers and shared memory.
+//
+// Construction, per warp.  Key of a draft node: (score, higher first; then
+// rank sequence, lexicographically smaller first).  Rank sequences are packed
+// four bits per depth, depth 1 in the top nibble, with the depths below the
+// node's own left at zero; comparing (packed value, depth) then orders rank
+// sequences exactly lexicographically with a prefix before its extensions.
+// Every node has at most two successors in the left-child / right-sibling
+// view of the tree: its first child (rank 0 one depth down) and its next
+// sibling (rank + 1 at its own depth).  Neither outranks the node (a
+// log-probability is <= 0 and each depth's list is best first; float32
+// rounding is monotone), so selecting the best node of a frontier that starts
+// at the best depth-1 node, and replacing each selected node by its two
+// successors, yields the nodes in exactly the ranking order.  The frontier
+// never holds more than budget + 1 <= 64 nodes: two per lane.  One step is a
+// warp-wide arg-max (five butterfly rounds), a broadcast of the winner, and
+// two insertions.
+#include <math.h>
+
+#include "common.cuh"
+#include "../../include/mla_ddtree.h"
+
+namespace mlav {
+namespace {
+
+constexpr int kTreeWarps = 4;  // sequences per CTA
+constexpr int kMaxDepth = MLA_DDTREE_MAX_DEPTH;
+constexpr int kMaxCand = MLA_DDTREE_MAX_CAND;
+
+static_assert(kMaxDepth * 4 <= 64 && kMaxCand <= 16, "rank sequences are packed 4 bits per depth");
+
+// Larger float (scores are <= 0 or -inf) -> larger key; +0 and -0 the same
+// key, as they compare equal.  0 is below every key of a valid node.
+__device__ __forceinline__ uint32_t score_key(float s) {
+  if (s == 0.0f) s = 0.0f;
+  const uint32_t u = __float_as_uint(s);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+struct Node {
+  uint32_t key;     // score_key(score); 0 = empty slot
+  uint64_t packed;  // rank sequence, depth 1 in bits 63..60
+  int depth, rank, parent;
+  float score, pscore;  // own score, parent's score
+};
+
+__device__ __forceinline__ int rank_shift(int depth) { return 4 * (kMaxDepth - depth); }
+
+// a outranks b (ties in key: smaller rank sequence; then the slot id, which
+// only orders empty slots, so all lanes agree on one winner)
+__device__ __forceinline__ bool outranks(uint32_t ka, uint64_t pa, int da, int ia, uint32_t kb, uint64_t pb, int db,
+                                         int ib) {
+  if (ka != kb) return ka > kb;
+  if (pa != pb) return pa < pb;
+  if (da != db) return da < db;
+  return ia < ib;
+}
+
+__device__ __forceinline__ Node shfl_node(const Node& n, int src) {
+  Node o;
+  o.key = __shfl_sync(0xffffffffu, n.key, src);
+  o.packed = __shfl_sync(0xffffffffu, n.packed, src);
+  o.depth = __shfl_sync(0xffffffffu, n.depth, src);
+  o.rank = __shfl_sync(0xffffffffu, n.rank, src);
+  o.parent = __shfl_sync(0xffffffffu, n.parent, src);
+  o.score = __shfl_sync(0xffffffffu, n.score, src);
+  o.pscore = __shfl_sync(0xffffffffu, n.pscore, src);
+  return o;
+}
+
+struct BuildParams {
+  int B, L, K, budget;
+  const int32_t* root_token;
+  const int32_t* cand_token;
+  const float* cand_logp;
+  int32_t* tree_parent;
+  int32_t* tree_token;
+  int32_t* tree_depth;
+  float* tree_score;
+  uint32_t* err;
+};
+
+__global__ void __launch_bounds__(kTreeWarps * 32) ddtree_build_kernel(BuildParams p) {
+  __shared__ float s_lp[kTreeWarps][kMaxDepth * kMaxCand];
+  __shared__ int32_t s_tok[kTreeWarps][kMaxDepth * kMaxCand];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int b = blockIdx.x * kTreeWarps + w;
+  if (b >= p.B) return;  // whole warp
+  const int LK = p.L * p.K, Q = p.budget + 1;
+  float* lp = s_lp[w];
+  int32_t* tok = s_tok[w];
+  const float* glp = p.cand_logp + (int64_t)b * LK;
+  const int32_t* gtok = p.cand_token + (int64_t)b * LK;
+  for (int i = lane; i < LK; i += 32) {
+    lp[i] = glp[i];
+    tok[i] = gtok[i];
+  }
+  __syncwarp();
+  bool bad = false;
+  for (int i = lane; i < LK; i += 32) {
+    const float v = lp[i];
+    bad |= isnan(v) || v > 0.0f || (i % p.K != 0 && v > lp[i - 1]);
+  }
+  if (__any_sync(0xffffffffu, bad)) {
+    if (lane == 0) set_err(p.err, MLA_DEVERR_DRAFT);
+    return;
+  }
+
+  const int64_t o = (int64_t)b * Q;
+  if (lane == 0) {
+    p.tree_parent[o] = -1;
+    p.tree_token[o] = p.root_token[b];
+    if (p.tree_depth) p.tree_depth[o] = 0;
+    if (p.tree_score) p.tree_score[o] = 0.0f;
+  }
+  // frontier slot ids: lane (f0) and 32 + lane (f1)
+  Node f0, f1;
+  f0.key = f1.key = 0;
+  f0.packed = f1.packed = 0;
+  f0.depth = f1.depth = f0.rank = f1.rank = f0.parent = f1.parent = 0;
+  f0.score = f1.score = f0.pscore = f1.pscore = 0.0f;
+  if (lane == 0) {  // the best depth-1 node
+    f0.score = 0.0f + lp[0];
+    f0.key = score_key(f0.score);
+    f0.depth = 1;
+  }
+  for (int n = 1; n < Q; ++n) {
+    // this lane's better slot, then the warp's best
+    const bool second = outranks(f1.key, f1.packed, f1.depth, 32 + lane, f0.key, f0.packed, f0.depth, lane);
+    uint32_t bk = second ? f1.key : f0.key;
+    uint64_t bp = second ? f1.packed : f0.packed;
+    int bd = second ? f1.depth : f0.depth;
+    int bi = second ? 32 + lane : lane;
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+      const uint32_t k2 = __shfl_xor_sync(0xffffffffu, bk, m);
+      const uint64_t p2 = __shfl_xor_sync(0xffffffffu, bp, m);
+      const int d2 = __shfl_xor_sync(0xffffffffu, bd, m);
+      const int i2 = __shfl_xor_sync(0xffffffffu, bi, m);
+      if (outranks(k2, p2, d2, i2, bk, bp, bd, bi)) {
+        bk = k2;
+        bp = p2;
+        bd = d2;
+        bi = i2;
+      }
+    }
+    if (bk == 0) {  // frontier exhausted: the host check on budget rules this out
+      if (lane == 0) set_err(p.err, MLA_DEVERR_DRAFT);
+      return;
+    }
+    const int wl = bi & 31, ws = bi >> 5;
+    const Node win = shfl_node(ws ? f1 : f0, wl);
+    if (lane == 0) {
+      p.tree_parent[o + n] = win.parent;
+      p.tree_token[o + n] = tok[(win.depth - 1) * p.K + win.rank];
+      if (p.tree_depth) p.tree_depth[o + n] = win.depth;
+      if (p.tree_score) p.tree_score[o + n] = win.score;
+    }
+    // the winner's slot takes its first child; the first empty slot its next sibling
+    if (lane == wl) {
+      Node c;
+      c.key = 0;
+      if (win.depth < p.L) {
+        c.score = win.score + lp[win.depth * p.K];
+        c.pscore = win.score;
+        c.key = score_key(c.score);
+        c.packed = win.packed;
+        c.depth = win.depth + 1;
+        c.rank = 0;
+        c.parent = n;
+      }
+      if (ws) {
+        if (c.key) f1 = c; else f1.key = 0;
+      } else {
+        if (c.key) f0 = c; else f0.key = 0;
+      }
+    }
+    if (win.rank + 1 < p.K) {
+      const unsigned e0 = __ballot_sync(0xffffffffu, f0.key == 0);
+      const unsigned e1 = __ballot_sync(0xffffffffu, f1.key == 0);
+      const int tl = e0 ? __ffs(e0) - 1 : __ffs(e1) - 1;
+      if (lane == tl && (e0 | e1)) {
+        Node c;
+        c.score = win.pscore + lp[(win.depth - 1) * p.K + win.rank + 1];
+        c.pscore = win.pscore;
+        c.key = score_key(c.score);
+        c.packed = win.packed + (1ull << rank_shift(win.depth));
+        c.depth = win.depth;
+        c.rank = win.rank + 1;
+        c.parent = win.parent;
+        if (e0) f0 = c; else f1 = c;
+      }
+    }
+  }
+}
+
+struct AcceptParams {
+  int B, Q;
+  const int32_t* tree_parent;
+  const int32_t* tree_token;
+  const int32_t* target_token;
+  const int32_t* node_slot;
+  int32_t* accept_len;
+  int32_t* accept_nodes;
+  int32_t* accept_slots;
+  int32_t* next_token;
+  uint32_t* err;
+};
+
+// One warp per sequence; node j sits in lane j & 31, register j >> 5.
+__global__ void __launch_bounds__(kTreeWarps * 32) ddtree_accept_kernel(AcceptParams p) {
+  __shared__ int32_t s_path[kTreeWarps][MLA_MAX_Q];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int b = blockIdx.x * kTreeWarps + w;
+  if (b >= p.B) return;
+  const int64_t o = (int64_t)b * p.Q;
+  int par[2], tk[2], tg[2];
+  bool bad = false;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = lane + 32 * h;
+    const bool in = j < p.Q;
+    par[h] = in ? p.tree_parent[o + j] : -2;
+    tk[h] = in ? p.tree_token[o + j] : 0;
+    tg[h] = in ? p.target_token[o + j] : 0;
+    if (in) bad |= (j == 0) ? par[h] != -1 : (par[h] < 0 || par[h] >= j);
+  }
+  if (__any_sync(0xffffffffu, bad)) {
+    if (lane == 0) set_err(p.err, MLA_DEVERR_PARENT);
+    return;
+  }
+  int32_t* path = s_path[w];
+  int cur = 0, len = 1;
+  if (lane == 0) path[0] = 0;
+  // parents precede children, so cur grows every step and the walk ends
+  for (;;) {
+    const int want = __shfl_sync(0xffffffffu, cur < 32 ? tg[0] : tg[1], cur & 31);
+    const unsigned m0 = __ballot_sync(0xffffffffu, par[0] == cur && tk[0] == want);
+    const unsigned m1 = __ballot_sync(0xffffffffu, par[1] == cur && tk[1] == want);
+    if (!(m0 | m1)) break;
+    cur = m0 ? __ffs(m0) - 1 : 32 + __ffs(m1) - 1;
+    if (lane == 0) path[len] = cur;
+    ++len;
+  }
+  __syncwarp();
+  const int bonus = __shfl_sync(0xffffffffu, cur < 32 ? tg[0] : tg[1], cur & 31);
+  for (int j = lane; j < p.Q; j += 32) {
+    const int v = j < len ? path[j] : -1;
+    p.accept_nodes[o + j] = v;
+    if (p.accept_slots) p.accept_slots[o + j] = j < len ? p.node_slot[o + v] : -1;
+  }
+  if (lane == 0) {
+    p.accept_len[b] = len;
+    p.next_token[b] = bonus;
+  }
+}
+
+bool aligned4(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; }
+
+mla_status check_ws(void* ws, size_t bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || bytes < MLA_DDTREE_WORKSPACE_BYTES)
+    return MLA_ERR_WORKSPACE;
+  return MLA_OK;
+}
+
+// K + K^2 + ... + K^L, saturated above the largest budget
+int64_t draft_nodes(int L, int K) {
+  int64_t total = 0, pw = 1;
+  for (int d = 1; d <= L; ++d) {
+    pw *= K;
+    total += pw;
+    if (total > MLA_DDTREE_MAX_BUDGET) return total;
+  }
+  return total;
+}
+
+}  // namespace
+}  // namespace mlav
+
+using namespace mlav;
+
+extern "C" mla_status mla_ddtree_build(const mla_ddtree_build_args* a, void* ws, size_t ws_bytes,
+                                       mla_stream_t stream) {
+  if (!a || a->B < 0) return MLA_ERR_INVALID_ARG;
+  if (a->L < 1 || a->L > kMaxDepth || a->K < 1 || a->K > kMaxCand) return MLA_ERR_INVALID_ARG;
+  if (a->budget < 1 || a->budget > MLA_DDTREE_MAX_BUDGET || a->budget > draft_nodes(a->L, a->K))
+    return MLA_ERR_INVALID_ARG;
+  const mla_status wst = check_ws(ws, ws_bytes);
+  if (wst != MLA_OK) return wst;
+  if (a->B == 0) return MLA_OK;
+  if (!a->root_token || !a->cand_token || !a->cand_logp || !a->tree_parent || !a->tree_token)
+    return MLA_ERR_INVALID_ARG;
+  const void* ptrs[] = {a->root_token, a->cand_token, a->cand_logp, a->tree_parent,
+                        a->tree_token, a->tree_depth, a->tree_score};
+  for (const void* q : ptrs)
+    if (!aligned4(q)) return MLA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, 16, st) != cudaSuccess) return MLA_ERR_CUDA;
+  BuildParams p;
+  p.B = a->B;
+  p.L = a->L;
+  p.K = a->K;
+  p.budget = a->budget;
+  p.root_token = a->root_token;
+  p.cand_token = a->cand_token;
+  p.cand_logp = a->cand_logp;
+  p.tree_parent = a->tree_parent;
+  p.tree_token = a->tree_token;
+  p.tree_depth = a->tree_depth;
+  p.tree_score = a->tree_score;
+  p.err = static_cast<uint32_t*>(ws);
+  const int grid = (a->B + kTreeWarps - 1) / kTreeWarps;
+  ddtree_build_kernel<<<grid, kTreeWarps * 32, 0, st>>>(p);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+extern "C" mla_status mla_ddtree_accept(const mla_ddtree_accept_args* a, void* ws, size_t ws_bytes,
+                                        mla_stream_t stream) {
+  if (!a || a->B < 0 || a->Q < 1 || a->Q > MLA_MAX_Q) return MLA_ERR_INVALID_ARG;
+  if (a->accept_slots && !a->node_slot) return MLA_ERR_INVALID_ARG;
+  const mla_status wst = check_ws(ws, ws_bytes);
+  if (wst != MLA_OK) return wst;
+  if (a->B == 0) return MLA_OK;
+  if (!a->tree_parent || !a->tree_token || !a->target_token || !a->accept_len || !a->accept_nodes ||
+      !a->next_token)
+    return MLA_ERR_INVALID_ARG;
+  const void* ptrs[] = {a->tree_parent, a->tree_token, a->target_token, a->node_slot,
+                        a->accept_len,  a->accept_nodes, a->accept_slots, a->next_token};
+  for (const void* q : ptrs)
+    if (!aligned4(q)) return MLA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, 16, st) != cudaSuccess) return MLA_ERR_CUDA;
+  AcceptParams p;
+  p.B = a->B;
+  p.Q = a->Q;
+  p.tree_parent = a->tree_parent;
+  p.tree_token = a->tree_token;
+  p.target_token = a->target_token;
+  p.node_slot = a->node_slot;
+  p.accept_len = a->accept_len;
+  p.accept_nodes = a->accept_nodes;
+  p.accept_slots = a->accept_slots;
+  p.next_token = a->next_token;
+  p.err = static_cast<uint32_t*>(ws);
+  const int grid = (a->B + kTreeWarps - 1) / kTreeWarps;
+  ddtree_accept_kernel<<<grid, kTreeWarps * 32, 0, st>>>(p);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}

@@ -121,3 +121,16 @@ def make_draft_config(name: str, seed: Optional[int] = None, mode: str = "softma
     if seed is not None:
         cfg["seed"] = seed
     return make_draft(name=name, mode=mode, **cfg)
+
+
+def random_rooted_tree(B: int, Q: int, seed: int, vocab: int = VOCAB):
+    """Trees of Q nodes with node 0 the only root (parent[i] uniform in [0, i-1])
+    and tokens drawn from ``vocab`` ids (a small vocab makes equal sibling
+    tokens common).  Returns (tree_parent, tree_token) [B][Q] int32."""
+    rng = np.random.default_rng(seed)
+    tp = np.zeros((B, Q), dtype=np.int32)
+    tt = rng.integers(0, vocab, size=(B, Q)).astype(np.int32)
+    tp[:, 0] = -1
+    for i in range(1, Q):
+        tp[:, i] = rng.integers(0, i, size=B)
+    return tp, tt

@@ -1,6 +1,7 @@
 """The C-ABI library without a GPU: it loads, exports every declared symbol,
 and rejects malformed arguments on the host before touching CUDA."""
 import ctypes
+import glob
 import os
 import re
 
@@ -9,7 +10,7 @@ import pytest
 from mla_tree_verify_absorbed_gb300 import api, build as B
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "mla_verify.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 @pytest.fixture(scope="module")
@@ -19,9 +20,11 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(mla_\w+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(mla_\w+)\s*\(", text))
+    return sorted(names)
 
 
 def test_exports_every_declared_symbol(lib):
@@ -170,3 +173,81 @@ def test_kv_compact_argument_checks(lib):
     assert call(s1=577) == api.MLA_ERR_INVALID_ARG              # row stride not a multiple of 16 bytes
     assert call(slot0=-1) == api.MLA_ERR_INVALID_ARG
     assert call(slots=1 << 40) == api.MLA_ERR_INVALID_ARG
+
+
+def fake_build_args(**kw):
+    a = api.MlaDdtreeBuildArgs()
+    a.B, a.L, a.K, a.budget = 4, 16, 8, 63
+    p = 0x10000
+    for f in ("root_token", "cand_token", "cand_logp", "tree_parent", "tree_token", "tree_depth", "tree_score"):
+        setattr(a, f, p)
+        p += 0x10000
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def fake_accept_args(**kw):
+    a = api.MlaDdtreeAcceptArgs()
+    a.B, a.Q = 4, 64
+    p = 0x10000
+    for f in ("tree_parent", "tree_token", "target_token", "node_slot", "accept_len", "accept_nodes",
+              "accept_slots", "next_token"):
+        setattr(a, f, p)
+        p += 0x10000
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_ddtree_struct_layout(lib):
+    A = api.MlaDdtreeBuildArgs
+    assert A.root_token.offset == 16 and A.tree_score.offset == 64 and ctypes.sizeof(A) == 72
+    C = api.MlaDdtreeAcceptArgs
+    assert C.tree_parent.offset == 8 and C.next_token.offset == 64 and ctypes.sizeof(C) == 72
+
+
+@pytest.mark.parametrize("field,value", [
+    ("B", -1), ("L", 0), ("L", 17), ("K", 0), ("K", 17), ("budget", 0), ("budget", 64),
+    ("root_token", 0), ("cand_token", 0), ("cand_logp", 0), ("tree_parent", 0), ("tree_token", 0),
+    ("cand_logp", 0x10002), ("tree_depth", 0x10001),
+])
+def test_ddtree_build_argument_checks(lib, field, value):
+    a = fake_build_args(**{field: value})
+    st = lib.mla_ddtree_build(ctypes.byref(a), ctypes.c_void_p(0x100000), ctypes.c_size_t(256), None)
+    assert st == api.MLA_ERR_INVALID_ARG
+
+
+def test_ddtree_build_budget_above_node_count(lib):
+    # K = 1, L = 4: only four draft nodes exist
+    a = fake_build_args(K=1, L=4, budget=5)
+    assert lib.mla_ddtree_build(ctypes.byref(a), ctypes.c_void_p(0x100000), 256, None) == api.MLA_ERR_INVALID_ARG
+    # K = 2, L = 2: 6 nodes
+    a = fake_build_args(K=2, L=2, budget=7)
+    assert lib.mla_ddtree_build(ctypes.byref(a), ctypes.c_void_p(0x100000), 256, None) == api.MLA_ERR_INVALID_ARG
+
+
+def test_ddtree_workspace_checks(lib):
+    a = fake_build_args()
+    for ws, n in ((0, 256), (0x100080, 256), (0x100000, 255)):
+        assert lib.mla_ddtree_build(ctypes.byref(a), ctypes.c_void_p(ws), n, None) == api.MLA_ERR_WORKSPACE
+    c = fake_accept_args()
+    for ws, n in ((0, 256), (0x100080, 256), (0x100000, 16)):
+        assert lib.mla_ddtree_accept(ctypes.byref(c), ctypes.c_void_p(ws), n, None) == api.MLA_ERR_WORKSPACE
+
+
+def test_ddtree_empty_batch_is_noop(lib):
+    a = fake_build_args(B=0)
+    assert lib.mla_ddtree_build(ctypes.byref(a), ctypes.c_void_p(0x100000), 256, None) == api.MLA_OK
+    c = fake_accept_args(B=0)
+    assert lib.mla_ddtree_accept(ctypes.byref(c), ctypes.c_void_p(0x100000), 256, None) == api.MLA_OK
+
+
+@pytest.mark.parametrize("field,value", [
+    ("B", -1), ("Q", 0), ("Q", 65), ("tree_parent", 0), ("tree_token", 0), ("target_token", 0),
+    ("accept_len", 0), ("accept_nodes", 0), ("next_token", 0), ("node_slot", 0), ("accept_nodes", 0x10002),
+])
+def test_ddtree_accept_argument_checks(lib, field, value):
+    c = fake_accept_args(**{field: value})
+    st = lib.mla_ddtree_accept(ctypes.byref(c), ctypes.c_void_p(0x100000), ctypes.c_size_t(256), None)
+    assert st == api.MLA_ERR_INVALID_ARG
