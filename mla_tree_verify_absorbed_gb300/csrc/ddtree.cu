@@ -24,8 +24,10 @@
 // at the best depth-1 node, and replacing each selected node by its two
 // successors, yields the nodes in exactly the ranking order.  The frontier
 // never holds more than budget + 1 <= 64 nodes: two per lane.  One step is a
-// warp-wide arg-max (five butterfly rounds), a broadcast of the winner, and
-// two insertions.
+// warp-wide max of the lanes' best score keys (one redux.sync; five butterfly
+// rounds on (rank sequence, depth) only when several lanes tie on score), a
+// broadcast of the winner, and two insertions.  The tree is staged in shared
+// memory and written out with coalesced stores at the end.
 #include <math.h>
 
 #include "common.cuh"
@@ -94,6 +96,8 @@ struct BuildParams {
 __global__ void __launch_bounds__(kTreeWarps * 32) ddtree_build_kernel(BuildParams p) {
   __shared__ float s_lp[kTreeWarps][kMaxDepth * kMaxCand];
   __shared__ int32_t s_tok[kTreeWarps][kMaxDepth * kMaxCand];
+  __shared__ int32_t s_par[kTreeWarps][MLA_MAX_Q], s_ntok[kTreeWarps][MLA_MAX_Q], s_dep[kTreeWarps][MLA_MAX_Q];
+  __shared__ float s_sc[kTreeWarps][MLA_MAX_Q];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int b = blockIdx.x * kTreeWarps + w;
   if (b >= p.B) return;  // whole warp
@@ -117,14 +121,19 @@ __global__ void __launch_bounds__(kTreeWarps * 32) ddtree_build_kernel(BuildPara
     return;
   }
 
-  const int64_t o = (int64_t)b * Q;
+  int32_t* o_par = s_par[w];
+  int32_t* o_tok = s_ntok[w];
+  int32_t* o_dep = s_dep[w];
+  float* o_sc = s_sc[w];
   if (lane == 0) {
-    p.tree_parent[o] = -1;
-    p.tree_token[o] = p.root_token[b];
-    if (p.tree_depth) p.tree_depth[o] = 0;
-    if (p.tree_score) p.tree_score[o] = 0.0f;
+    o_par[0] = -1;
+    o_tok[0] = p.root_token[b];
+    o_dep[0] = 0;
+    o_sc[0] = 0.0f;
   }
-  // frontier slot ids: lane (f0) and 32 + lane (f1)
+  // Frontier slot s lives in lane s & 31, register s >> 5 (f0 / f1).  A
+  // selected node's first child reuses its slot; its next sibling takes slot
+  // `next_free`, which only grows: 1 + (one per step) <= 1 + budget <= 64.
   Node f0, f1;
   f0.key = f1.key = 0;
   f0.packed = f1.packed = 0;
@@ -135,39 +144,45 @@ __global__ void __launch_bounds__(kTreeWarps * 32) ddtree_build_kernel(BuildPara
     f0.key = score_key(f0.score);
     f0.depth = 1;
   }
+  int next_free = 1;
   for (int n = 1; n < Q; ++n) {
-    // this lane's better slot, then the warp's best
+    // this lane's better slot (full key), then the warp's highest score key
     const bool second = outranks(f1.key, f1.packed, f1.depth, 32 + lane, f0.key, f0.packed, f0.depth, lane);
-    uint32_t bk = second ? f1.key : f0.key;
-    uint64_t bp = second ? f1.packed : f0.packed;
-    int bd = second ? f1.depth : f0.depth;
-    int bi = second ? 32 + lane : lane;
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) {
-      const uint32_t k2 = __shfl_xor_sync(0xffffffffu, bk, m);
-      const uint64_t p2 = __shfl_xor_sync(0xffffffffu, bp, m);
-      const int d2 = __shfl_xor_sync(0xffffffffu, bd, m);
-      const int i2 = __shfl_xor_sync(0xffffffffu, bi, m);
-      if (outranks(k2, p2, d2, i2, bk, bp, bd, bi)) {
-        bk = k2;
-        bp = p2;
-        bd = d2;
-        bi = i2;
-      }
-    }
-    if (bk == 0) {  // frontier exhausted: the host check on budget rules this out
+    const uint32_t lk = second ? f1.key : f0.key;
+    const uint32_t top = __reduce_max_sync(0xffffffffu, lk);
+    if (top == 0) {  // frontier exhausted: the host check on budget rules this out
       if (lane == 0) set_err(p.err, MLA_DEVERR_DRAFT);
       return;
     }
-    const int wl = bi & 31, ws = bi >> 5;
-    const Node win = shfl_node(ws ? f1 : f0, wl);
-    if (lane == 0) {
-      p.tree_parent[o + n] = win.parent;
-      p.tree_token[o + n] = tok[(win.depth - 1) * p.K + win.rank];
-      if (p.tree_depth) p.tree_depth[o + n] = win.depth;
-      if (p.tree_score) p.tree_score[o + n] = win.score;
+    const unsigned tied = __ballot_sync(0xffffffffu, lk == top);
+    int wl = __ffs(tied) - 1;
+    if (tied & (tied - 1)) {
+      // equal scores in several lanes: the smallest (rank sequence, depth) wins
+      uint64_t bp = lk == top ? (second ? f1.packed : f0.packed) : ~0ull;
+      int bd = lk == top ? (second ? f1.depth : f0.depth) : 0x7fffffff;
+      int bi = lane;
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) {
+        const uint64_t p2 = __shfl_xor_sync(0xffffffffu, bp, m);
+        const int d2 = __shfl_xor_sync(0xffffffffu, bd, m);
+        const int i2 = __shfl_xor_sync(0xffffffffu, bi, m);
+        if (p2 < bp || (p2 == bp && (d2 < bd || (d2 == bd && i2 < bi)))) {
+          bp = p2;
+          bd = d2;
+          bi = i2;
+        }
+      }
+      wl = bi;
     }
-    // the winner's slot takes its first child; the first empty slot its next sibling
+    const bool ws = __shfl_sync(0xffffffffu, second, wl);
+    const Node win = shfl_node(second ? f1 : f0, wl);
+    if (lane == 0) {
+      o_par[n] = win.parent;
+      o_tok[n] = tok[(win.depth - 1) * p.K + win.rank];
+      o_dep[n] = win.depth;
+      o_sc[n] = win.score;
+    }
+    // the winner's slot takes its first child (or empties)
     if (lane == wl) {
       Node c;
       c.key = 0;
@@ -186,11 +201,9 @@ __global__ void __launch_bounds__(kTreeWarps * 32) ddtree_build_kernel(BuildPara
         if (c.key) f0 = c; else f0.key = 0;
       }
     }
+    // its next sibling takes a fresh slot
     if (win.rank + 1 < p.K) {
-      const unsigned e0 = __ballot_sync(0xffffffffu, f0.key == 0);
-      const unsigned e1 = __ballot_sync(0xffffffffu, f1.key == 0);
-      const int tl = e0 ? __ffs(e0) - 1 : __ffs(e1) - 1;
-      if (lane == tl && (e0 | e1)) {
+      if (lane == (next_free & 31)) {
         Node c;
         c.score = win.pscore + lp[(win.depth - 1) * p.K + win.rank + 1];
         c.pscore = win.pscore;
@@ -199,9 +212,18 @@ __global__ void __launch_bounds__(kTreeWarps * 32) ddtree_build_kernel(BuildPara
         c.depth = win.depth;
         c.rank = win.rank + 1;
         c.parent = win.parent;
-        if (e0) f0 = c; else f1 = c;
+        if (next_free >> 5) f1 = c; else f0 = c;
       }
+      ++next_free;
     }
+  }
+  __syncwarp();
+  const int64_t o = (int64_t)b * Q;
+  for (int j = lane; j < Q; j += 32) {
+    p.tree_parent[o + j] = o_par[j];
+    p.tree_token[o + j] = o_tok[j];
+    if (p.tree_depth) p.tree_depth[o + j] = o_dep[j];
+    if (p.tree_score) p.tree_score[o + j] = o_sc[j];
   }
 }
 
