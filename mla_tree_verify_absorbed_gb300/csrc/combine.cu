@@ -37,7 +37,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   // pass 2: weights exp(lse_k - M) (lane k % 32 holds piece k's), warp sum, and
-  // the weighted sum of the pieces' outputs, four pieces' loads in flight
+  // the weighted sum of the pieces' outputs in piece order.  The loads of
+  // kBatch pieces are issued before any is used; a piece with weight 0 (empty,
+  // or beyond S) loads from piece k0, which is always allocated, and its value
+  // is never used, so nothing it holds reaches the sum.
+  constexpr int kBatch = 8;
   float L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != -INFINITY) {
@@ -49,16 +53,24 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
       for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
       L += wsum;
       const int n = S - k0 < 32 ? S - k0 : 32;
-#pragma unroll 4
-      for (int q = 0; q < n; ++q) {
-        const float w = __shfl_sync(0xffffffffu, wk, q);
-        if (w != 0.f) {
-          const float4 v = reinterpret_cast<const float4*>(p.part_o + (item_of(k0 + q) * p.rg + r) * kDl)
-              [quarter * 32 + lane];
-          acc.x = fmaf(w, v.x, acc.x);
-          acc.y = fmaf(w, v.y, acc.y);
-          acc.z = fmaf(w, v.z, acc.z);
-          acc.w = fmaf(w, v.w, acc.w);
+      for (int q0 = 0; q0 < n; q0 += kBatch) {
+        float w[kBatch];
+        float4 v[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          w[u] = __shfl_sync(0xffffffffu, wk, (q0 + u) & 31);
+          if (q0 + u >= n) w[u] = 0.f;
+          const int kk = w[u] != 0.f ? k0 + q0 + u : k0;
+          v[u] = reinterpret_cast<const float4*>(p.part_o + (item_of(kk) * p.rg + r) * kDl)[quarter * 32 + lane];
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          if (w[u] != 0.f) {
+            acc.x = fmaf(w[u], v[u].x, acc.x);
+            acc.y = fmaf(w[u], v[u].y, acc.y);
+            acc.z = fmaf(w[u], v[u].z, acc.z);
+            acc.w = fmaf(w[u], v[u].w, acc.w);
+          }
         }
       }
     }

@@ -6,9 +6,10 @@
 // Anchored a Complex CUDA Kernel Implementation", section "Output Knowledge
 // Created by This Message" (prefix visibility + tree-tail visibility) and
 // "Ground Truth in Silicon ...", section "Input Knowledge Required ...",
-// item 3: node i sees tree node t when t is i or an ancestor of i.  With nodes
-// in topological order (parent[i] < i) the set is built in one forward pass:
-// anc[i] = bit(i) | anc[parent[i]].
+// item 3: node i sees tree node t when t is i or an ancestor of i.  One thread
+// per (sequence, node) walks the node's parent links and sets a bit for each
+// ancestor; parents precede their nodes, so the walk takes at most i steps, and
+// a link that breaks that rule ends the walk (its own node reports it).
 #include "common.cuh"
 
 namespace mlav {
@@ -32,8 +33,9 @@ __device__ int64_t block_inclusive_scan(int64_t v, int64_t* sh) {
 }
 
 // One block.  Clears the error word, validates prefix_lens / kv_indptr /
-// page capacity / parents, builds anc, T_b = ceil(N_b / tk), and the prefix
-// sums seq_kv_base of N_b.
+// page capacity, computes T_b = ceil(N_b / tk) and the prefix sums
+// seq_kv_base of N_b (a thread per sequence), then validates the parents and
+// builds anc (a thread per node).
 __global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
   __shared__ int64_t sh[kMetaThreads];
   __shared__ int64_t carry_kv;
@@ -62,15 +64,6 @@ __global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
       } else if (N > (int64_t)p.max_pages * p.page_size) {
         e |= MLA_DEVERR_PAGES;
       }
-      // ancestor-or-self masks
-      uint64_t anc_local[MLA_MAX_Q];
-      for (int i = 0; i < p.Q; ++i) {
-        int par = p.tree_parent[(int64_t)b * p.Q + i];
-        if (par < -1 || par >= i) { e |= MLA_DEVERR_PARENT; par = -1; }
-        const uint64_t self = 1ull << i;
-        anc_local[i] = (par < 0) ? self : (anc_local[par] | self);
-        p.anc[(int64_t)b * p.Q + i] = anc_local[i];
-      }
       if (e) set_err(p.err, e);
       const int64_t T = (N + p.tk - 1) / p.tk;
       p.seq_tiles[b] = (int32_t)T;
@@ -86,6 +79,25 @@ __global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
     }
     __syncthreads();
   }
+
+  // ancestor-or-self masks
+  const int64_t nodes = (int64_t)p.B * p.Q;
+  uint32_t e = 0;
+  for (int64_t k = tid; k < nodes; k += kMetaThreads) {
+    const int i = (int)(k % p.Q);
+    const int32_t* par = p.tree_parent + (k - i);
+    int j = par[i];
+    if (j < -1 || j >= i) e |= MLA_DEVERR_PARENT;
+    uint64_t m = 1ull << i;
+    int cur = i;
+    while (j >= 0 && j < cur) {
+      m |= 1ull << j;
+      cur = j;
+      j = par[j];
+    }
+    p.anc[k] = m;
+  }
+  if (e) set_err(p.err, e);
 }
 
 // Grid-stride pass over every (sequence, position): checks that each resolved
