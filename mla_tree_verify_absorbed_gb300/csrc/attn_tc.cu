@@ -713,13 +713,9 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads,
   uint8_t* smem = smem_raw;
   const uint32_t rank = cluster_ctarank();
   const int warp = threadIdx.x >> 5;
-  // All CTAs of a cluster must take the same branch here.  The validation bits
-  // were final before this kernel started; the timeout bit may be raised by
-  // another cluster while this one starts, so it is not part of the test.
-  if ((*p.err & ~MLA_DEVERR_TIMEOUT) || (smem_u32(smem) & 1023u)) {
-    if (threadIdx.x == 0 && (smem_u32(smem) & 1023u)) set_err(p.err, MLA_DEVERR_LAYOUT);
-    return;
-  }
+  // The prologue (barriers, Tensor Memory, cluster sync) touches only this
+  // cluster's shared and Tensor Memory, so it may overlap the end of the
+  // metadata kernel; everything after grid_dep_wait() reads its results.
   Ctl* c = reinterpret_cast<Ctl*>(smem + kOffCtl);
   const bool leader = (rank & 1) == 0;
   if (threadIdx.x == 0) {
@@ -754,6 +750,17 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads,
   tc_fence_before();
   cluster_sync();  // barriers of all CTAs initialised before any remote use
   tc_fence_after();
+  grid_dep_wait();
+  // All CTAs of a cluster take the same branch here.  The validation bits are
+  // final once the metadata kernel has completed; the timeout bit may be
+  // raised by another cluster meanwhile, so it is not part of the test.
+  if ((*p.err & ~MLA_DEVERR_TIMEOUT) || (smem_u32(smem) & 1023u)) {
+    if (threadIdx.x == 0 && (smem_u32(smem) & 1023u)) set_err(p.err, MLA_DEVERR_LAYOUT);
+    tc_fence_before();
+    cluster_sync();
+    if (warp == kWarpAux) tmem_dealloc_pair(c->tmem_base, kTmemCols);
+    return;
+  }
 
   const int cluster_id = blockIdx.x / kClusterCtas;
   const int n_clusters = gridDim.x / kClusterCtas;
@@ -775,6 +782,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads,
   }
 
   __syncwarp();
+  grid_dep_launch();  // the LSE combine may start launching; it waits for this grid
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0 && c->abort) {
@@ -811,12 +819,12 @@ int tc_clusters_per_gpu(int sm_count) {
   return n;
 }
 
-cudaError_t launch_attn_tc(const Params& p, cudaStream_t stream) {
+cudaError_t launch_attn_tc(const Params& p, cudaStream_t stream, bool pdl) {
   cudaError_t e = cudaFuncSetAttribute(tc::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        tc::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  tc::attn_tc_kernel<<<tc::kClusterCtas * p.grid, tc::kThreads, tc::kSmemAlloc, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(tc::attn_tc_kernel, dim3(tc::kClusterCtas * p.grid), dim3(tc::kThreads), tc::kSmemAlloc,
+                       stream, pdl, p);
 }
 
 }  // namespace mlav

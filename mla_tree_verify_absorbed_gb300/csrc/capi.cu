@@ -12,10 +12,10 @@ namespace mlav {
 cudaError_t launch_meta(const Params& p, int sm_count, int32_t* slots_out, int64_t capacity,
                         uint64_t* anc_out, cudaStream_t stream);
 cudaError_t launch_attn_simt(const Params& p, cudaStream_t stream);
-cudaError_t launch_combine(const Params& p, cudaStream_t stream);
+cudaError_t launch_combine(const Params& p, cudaStream_t stream, bool pdl);
 int simt_rows_per_group();
 int simt_tokens_per_tile();
-cudaError_t launch_attn_tc(const Params& p, cudaStream_t stream);
+cudaError_t launch_attn_tc(const Params& p, cudaStream_t stream, bool pdl);
 int tc_rows_per_group();
 int tc_tokens_per_tile();
 int tc_clusters_per_gpu(int sm_count);
@@ -237,13 +237,17 @@ mla_status run_attn(const mla_verify_args* a, void* workspace, size_t ws_bytes, 
   Params p = make_params(a, pl, workspace);
   p.hold_ns = hold_ns;
   if (launch_meta(p, pl.sm_count, nullptr, 0, nullptr, s) != cudaSuccess) return MLA_ERR_CUDA;
+  // Consecutive kernels overlap launch and prologue with the previous kernel's
+  // tail (programmatic dependent launch), except around the caller's profiling
+  // events, which must see each kernel start and end on its own.
+  const bool pdl = a->profile_events == nullptr;
   if (a->profile_events && cudaEventRecord((cudaEvent_t)a->profile_events[0], s) != cudaSuccess)
     return MLA_ERR_CUDA;
-  cudaError_t e = (pl.algo == MLA_ALGO_TC) ? launch_attn_tc(p, s) : launch_attn_simt(p, s);
+  cudaError_t e = (pl.algo == MLA_ALGO_TC) ? launch_attn_tc(p, s, pdl) : launch_attn_simt(p, s);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   if (a->profile_events && cudaEventRecord((cudaEvent_t)a->profile_events[1], s) != cudaSuccess)
     return MLA_ERR_CUDA;
-  if (pl.splits > 1 && launch_combine(p, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (pl.splits > 1 && launch_combine(p, s, pdl) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }
 }  // namespace

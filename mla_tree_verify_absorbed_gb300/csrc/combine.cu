@@ -15,6 +15,7 @@ constexpr int kCombineThreads = 256;  // 8 warps; one warp per (row, quarter of 
 constexpr int kQuarters = 4;          // 128 columns per warp: one float4 per lane
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
+  grid_dep_wait();  // the attention kernel's partials and error word
   if (*p.err) return;
   const int lane = threadIdx.x & 31;
   const int64_t gw = (int64_t)blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5);
@@ -92,12 +93,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   if (quarter == 0 && lane == 0 && p.lse) p.lse[orow] = (L > 0.f) ? M + logf(L) : -INFINITY;
 }
 
-cudaError_t launch_combine(const Params& p, cudaStream_t stream) {
+cudaError_t launch_combine(const Params& p, cudaStream_t stream, bool pdl) {
   const int64_t warps = (int64_t)p.B * p.rows * kQuarters;
   const int64_t blocks = (warps + (kCombineThreads / 32) - 1) / (kCombineThreads / 32);
   if (blocks == 0) return cudaSuccess;
-  combine_kernel<<<(unsigned)blocks, kCombineThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(combine_kernel, dim3((unsigned)blocks), dim3(kCombineThreads), 0, stream, pdl, p);
 }
 
 }  // namespace mlav

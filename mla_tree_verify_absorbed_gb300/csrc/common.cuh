@@ -7,6 +7,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/mla_verify.h"
 
 namespace mlav {
@@ -89,6 +91,34 @@ inline WsLayout ws_layout(int B, int Q, int rg, int64_t part_slots) {
 // Device helpers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void set_err(uint32_t* err, uint32_t bits) { atomicOr(err, bits); }
+
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the kernel before it in the stream is still
+// running; grid_dep_wait() blocks until that kernel has completed and its
+// writes are visible (it returns at once when the launch had no such
+// dependency).  grid_dep_launch() lets the next kernel start launching once
+// every CTA of this grid has called it or exited.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch with or without programmatic stream serialization.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                 bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Pool slot of logical position `pos` of sequence b.  The metadata kernel has
 // validated every table entry before any attention kernel runs; the clamps

@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
   __shared__ int64_t sh[kMetaThreads];
   __shared__ int64_t carry_kv;
   const int tid = threadIdx.x;
+  grid_dep_launch();  // the slot pass may start launching; it waits for this kernel
   if (tid == 0) {
     p.err[0] = 0u;
     p.err[1] = 0u;  // where a bounded wait gave up, if one did
@@ -105,6 +106,8 @@ __global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
 // table reads if the sequence-level checks already failed (an inconsistent
 // indptr would make the index arithmetic itself unsafe).
 __global__ void meta_slots_kernel(Params p, int32_t* slots_out, int64_t capacity) {
+  grid_dep_wait();    // reads the sequence metadata and error word of meta_seq_kernel
+  grid_dep_launch();  // the attention kernel may start its prologue meanwhile
   if (*p.err & (MLA_DEVERR_PREFIX | MLA_DEVERR_INDPTR | MLA_DEVERR_PAGES)) return;
   const int64_t total = p.seq_kv_base[p.B];
   uint32_t e = 0;
@@ -140,8 +143,7 @@ cudaError_t launch_meta(const Params& p, int sm_count, int32_t* slots_out, int64
   meta_seq_kernel<<<1, kMetaThreads, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  meta_slots_kernel<<<2 * sm_count, 256, 0, stream>>>(p, slots_out, capacity);
-  e = cudaGetLastError();
+  e = launch_kernel(meta_slots_kernel, dim3(2 * sm_count), dim3(256), 0, stream, true, p, slots_out, capacity);
   if (e != cudaSuccess) return e;
   if (anc_out) {
     copy_anc_kernel<<<64, 256, 0, stream>>>(p, anc_out);
