@@ -78,6 +78,13 @@ def barrier(dist):
         dist.barrier()
 
 
+def job_us_per_call(ms_per_step: float, world: int) -> float:
+    """Whole-job figure of the replicas: each of the `world` ranks completes one
+    call per step, so the job completes `world` calls in the slowest rank's
+    step time."""
+    return ms_per_step * 1000.0 / world
+
+
 def max_over_ranks(dist, x: float, device="cpu") -> float:
     if dist is None:
         return x
@@ -351,7 +358,7 @@ def run_ours(args):
         return 0
 
     ms_step = elapsed_ms / args.steps
-    us_call = ms_step * 1000.0 / world
+    us_call = job_us_per_call(ms_step, world)
     kernel_s = attn_avg_ms / 1000.0
     eff_kv_gbs = cnt["kv_bytes"] / (ms_step / 1000.0) / 1e9
     resolved = "simt" if algo == "simt" else "tc"   # AUTO takes the tensor-core kernel for bf16
@@ -549,7 +556,7 @@ def run_graph(args, p, di, dev, stream, algo, dist):
     barrier(dist)
     ms = max_over_ranks(dist, a.elapsed_time(b), device=dev)
     world = dist.get_world_size() if dist is not None else 1
-    return {"value": ms * 1000.0 / args.steps / world, "unit": UNIT, "note": "CUDA graph replay"}
+    return {"value": job_us_per_call(ms / args.steps, world), "unit": UNIT, "note": "CUDA graph replay"}
 
 
 def run_e2e(args, p, di, dev, stream, algo, dist):
@@ -593,7 +600,7 @@ def run_e2e(args, p, di, dev, stream, algo, dist):
     barrier(dist)
     ms = max_over_ranks(dist, a.elapsed_time(b), device=dev)
     world = dist.get_world_size() if dist is not None else 1
-    return {"value": ms * 1000.0 / args.steps / world, "unit": UNIT,
+    return {"value": job_us_per_call(ms / args.steps, world), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
