@@ -23,11 +23,15 @@
 // rounding is monotone), so selecting the best node of a frontier that starts
 // at the best depth-1 node, and replacing each selected node by its two
 // successors, yields the nodes in exactly the ranking order.  The frontier
-// never holds more than budget + 1 <= 64 nodes: two per lane.  One step is a
-// warp-wide max of the lanes' best score keys (one redux.sync; five butterfly
-// rounds on (rank sequence, depth) only when several lanes tie on score), a
-// broadcast of the winner, and two insertions.  The tree is staged in shared
-// memory and written out with coalesced stores at the end.
+// never holds more than budget + 1 <= 64 nodes.  A single warp has nothing to
+// hide the latency of dependent instructions, so a step is kept short: the
+// frontier lives in shared memory (one entry per slot) and each lane holds
+// only the score keys of its two slots; one redux.sync max and two ballots
+// name the winner (five butterfly rounds on (rank sequence, depth) only when
+// several slots tie on score); every lane reads the winner's entry and
+// computes its successors, so the arithmetic is uniform and only the writes
+// are predicated.  The tree is staged in shared memory and written out with
+// coalesced stores at the end.
 #include <math.h>
 
 #include "common.cuh"
@@ -50,36 +54,19 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-struct Node {
-  uint32_t key;     // score_key(score); 0 = empty slot
-  uint64_t packed;  // rank sequence, depth 1 in bits 63..60
-  int depth, rank, parent;
-  float score, pscore;  // own score, parent's score
-};
-
 __device__ __forceinline__ int rank_shift(int depth) { return 4 * (kMaxDepth - depth); }
 
-// a outranks b (ties in key: smaller rank sequence; then the slot id, which
-// only orders empty slots, so all lanes agree on one winner)
-__device__ __forceinline__ bool outranks(uint32_t ka, uint64_t pa, int da, int ia, uint32_t kb, uint64_t pb, int db,
-                                         int ib) {
-  if (ka != kb) return ka > kb;
-  if (pa != pb) return pa < pb;
-  if (da != db) return da < db;
-  return ia < ib;
-}
-
-__device__ __forceinline__ Node shfl_node(const Node& n, int src) {
-  Node o;
-  o.key = __shfl_sync(0xffffffffu, n.key, src);
-  o.packed = __shfl_sync(0xffffffffu, n.packed, src);
-  o.depth = __shfl_sync(0xffffffffu, n.depth, src);
-  o.rank = __shfl_sync(0xffffffffu, n.rank, src);
-  o.parent = __shfl_sync(0xffffffffu, n.parent, src);
-  o.score = __shfl_sync(0xffffffffu, n.score, src);
-  o.pscore = __shfl_sync(0xffffffffu, n.pscore, src);
-  return o;
-}
+// The frontier of one sequence, one entry per slot (64 slots), in shared
+// memory; each lane keeps the score keys of its two slots (lane, 32 + lane) in
+// registers.
+struct Frontier {
+  float score[MLA_MAX_Q];
+  float pscore[MLA_MAX_Q];  // the parent's score
+  uint64_t packed[MLA_MAX_Q];
+  int32_t depth[MLA_MAX_Q];
+  int32_t rank[MLA_MAX_Q];
+  int32_t parent[MLA_MAX_Q];
+};
 
 struct BuildParams {
   int B, L, K, budget;
@@ -98,12 +85,14 @@ __global__ void __launch_bounds__(kTreeWarps * 32) ddtree_build_kernel(BuildPara
   __shared__ int32_t s_tok[kTreeWarps][kMaxDepth * kMaxCand];
   __shared__ int32_t s_par[kTreeWarps][MLA_MAX_Q], s_ntok[kTreeWarps][MLA_MAX_Q], s_dep[kTreeWarps][MLA_MAX_Q];
   __shared__ float s_sc[kTreeWarps][MLA_MAX_Q];
+  __shared__ Frontier s_fr[kTreeWarps];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int b = blockIdx.x * kTreeWarps + w;
   if (b >= p.B) return;  // whole warp
   const int LK = p.L * p.K, Q = p.budget + 1;
   float* lp = s_lp[w];
   int32_t* tok = s_tok[w];
+  Frontier& fr = s_fr[w];
   const float* glp = p.cand_logp + (int64_t)b * LK;
   const int32_t* gtok = p.cand_token + (int64_t)b * LK;
   for (int i = lane; i < LK; i += 32) {
@@ -130,37 +119,51 @@ __global__ void __launch_bounds__(kTreeWarps * 32) ddtree_build_kernel(BuildPara
     o_tok[0] = p.root_token[b];
     o_dep[0] = 0;
     o_sc[0] = 0.0f;
+    // slot 0: the best depth-1 node
+    fr.score[0] = 0.0f + lp[0];
+    fr.pscore[0] = 0.0f;
+    fr.packed[0] = 0;
+    fr.depth[0] = 1;
+    fr.rank[0] = 0;
+    fr.parent[0] = 0;
   }
-  // Frontier slot s lives in lane s & 31, register s >> 5 (f0 / f1).  A
-  // selected node's first child reuses its slot; its next sibling takes slot
-  // `next_free`, which only grows: 1 + (one per step) <= 1 + budget <= 64.
-  Node f0, f1;
-  f0.key = f1.key = 0;
-  f0.packed = f1.packed = 0;
-  f0.depth = f1.depth = f0.rank = f1.rank = f0.parent = f1.parent = 0;
-  f0.score = f1.score = f0.pscore = f1.pscore = 0.0f;
-  if (lane == 0) {  // the best depth-1 node
-    f0.score = 0.0f + lp[0];
-    f0.key = score_key(f0.score);
-    f0.depth = 1;
-  }
+  // score keys of slots lane and 32 + lane (0 = empty).  A selected node's
+  // first child reuses its slot; its next sibling takes slot `next_free`,
+  // which only grows: 1 + (one per step) <= 1 + budget <= 64.
+  uint32_t k0 = 0, k1 = 0;
+  if (lane == 0) k0 = score_key(0.0f + lp[0]);
+  __syncwarp();
   int next_free = 1;
   for (int n = 1; n < Q; ++n) {
-    // this lane's better slot (full key), then the warp's highest score key
-    const bool second = outranks(f1.key, f1.packed, f1.depth, 32 + lane, f0.key, f0.packed, f0.depth, lane);
-    const uint32_t lk = second ? f1.key : f0.key;
+    const uint32_t lk = k0 > k1 ? k0 : k1;
     const uint32_t top = __reduce_max_sync(0xffffffffu, lk);
     if (top == 0) {  // frontier exhausted: the host check on budget rules this out
       if (lane == 0) set_err(p.err, MLA_DEVERR_DRAFT);
       return;
     }
-    const unsigned tied = __ballot_sync(0xffffffffu, lk == top);
-    int wl = __ffs(tied) - 1;
-    if (tied & (tied - 1)) {
-      // equal scores in several lanes: the smallest (rank sequence, depth) wins
-      uint64_t bp = lk == top ? (second ? f1.packed : f0.packed) : ~0ull;
-      int bd = lk == top ? (second ? f1.depth : f0.depth) : 0x7fffffff;
-      int bi = lane;
+    const unsigned t0 = __ballot_sync(0xffffffffu, k0 == top);
+    const unsigned t1 = __ballot_sync(0xffffffffu, k1 == top);
+    int win;  // slot of the selected node
+    if (__popc(t0) + __popc(t1) == 1) {
+      win = t0 ? __ffs(t0) - 1 : 32 + __ffs(t1) - 1;
+    } else {
+      // equal scores: the smallest (rank sequence, depth) wins
+      uint64_t bp = ~0ull;
+      int bd = 0x7fffffff, bi = 64;
+      if (k0 == top) {
+        bp = fr.packed[lane];
+        bd = fr.depth[lane];
+        bi = lane;
+      }
+      if (k1 == top) {
+        const uint64_t p1 = fr.packed[32 + lane];
+        const int d1 = fr.depth[32 + lane];
+        if (p1 < bp || (p1 == bp && d1 < bd)) {
+          bp = p1;
+          bd = d1;
+          bi = 32 + lane;
+        }
+      }
 #pragma unroll
       for (int m = 16; m >= 1; m >>= 1) {
         const uint64_t p2 = __shfl_xor_sync(0xffffffffu, bp, m);
@@ -172,50 +175,50 @@ __global__ void __launch_bounds__(kTreeWarps * 32) ddtree_build_kernel(BuildPara
           bi = i2;
         }
       }
-      wl = bi;
+      win = bi;
     }
-    const bool ws = __shfl_sync(0xffffffffu, second, wl);
-    const Node win = shfl_node(second ? f1 : f0, wl);
+    // every lane reads the winner and computes its successors (uniform values)
+    const float wsc = fr.score[win], wps = fr.pscore[win];
+    const uint64_t wpk = fr.packed[win];
+    const int wd = fr.depth[win], wr = fr.rank[win], wpar = fr.parent[win];
+    const bool has_child = wd < p.L, has_sib = wr + 1 < p.K;
+    const float csc = has_child ? wsc + lp[wd * p.K] : 0.0f;
+    const float ssc = has_sib ? wps + lp[(wd - 1) * p.K + wr + 1] : 0.0f;
+    const uint32_t ckey = has_child ? score_key(csc) : 0u;
+    const uint32_t skey = has_sib ? score_key(ssc) : 0u;
+    const int sslot = next_free;
+    __syncwarp();  // all reads of the winner's entry precede the writes below
     if (lane == 0) {
-      o_par[n] = win.parent;
-      o_tok[n] = tok[(win.depth - 1) * p.K + win.rank];
-      o_dep[n] = win.depth;
-      o_sc[n] = win.score;
-    }
-    // the winner's slot takes its first child (or empties)
-    if (lane == wl) {
-      Node c;
-      c.key = 0;
-      if (win.depth < p.L) {
-        c.score = win.score + lp[win.depth * p.K];
-        c.pscore = win.score;
-        c.key = score_key(c.score);
-        c.packed = win.packed;
-        c.depth = win.depth + 1;
-        c.rank = 0;
-        c.parent = n;
+      o_par[n] = wpar;
+      o_tok[n] = tok[(wd - 1) * p.K + wr];
+      o_dep[n] = wd;
+      o_sc[n] = wsc;
+      if (has_child) {
+        fr.score[win] = csc;
+        fr.pscore[win] = wsc;
+        fr.depth[win] = wd + 1;
+        fr.rank[win] = 0;
+        fr.parent[win] = n;  // packed unchanged: rank 0 at the new depth
       }
-      if (ws) {
-        if (c.key) f1 = c; else f1.key = 0;
-      } else {
-        if (c.key) f0 = c; else f0.key = 0;
+      if (has_sib) {
+        fr.score[sslot] = ssc;
+        fr.pscore[sslot] = wps;
+        fr.packed[sslot] = wpk + (1ull << rank_shift(wd));
+        fr.depth[sslot] = wd;
+        fr.rank[sslot] = wr + 1;
+        fr.parent[sslot] = wpar;
       }
     }
-    // its next sibling takes a fresh slot
-    if (win.rank + 1 < p.K) {
-      if (lane == (next_free & 31)) {
-        Node c;
-        c.score = win.pscore + lp[(win.depth - 1) * p.K + win.rank + 1];
-        c.pscore = win.pscore;
-        c.key = score_key(c.score);
-        c.packed = win.packed + (1ull << rank_shift(win.depth));
-        c.depth = win.depth;
-        c.rank = win.rank + 1;
-        c.parent = win.parent;
-        if (next_free >> 5) f1 = c; else f0 = c;
+    if (lane == (win & 31)) {
+      if (win >> 5) k1 = ckey; else k0 = ckey;
+    }
+    if (has_sib) {
+      if (lane == (sslot & 31)) {
+        if (sslot >> 5) k1 = skey; else k0 = skey;
       }
       ++next_free;
     }
+    __syncwarp();  // the frontier writes are visible to the next step's reads
   }
   __syncwarp();
   const int64_t o = (int64_t)b * Q;
