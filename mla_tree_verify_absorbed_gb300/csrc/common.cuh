@@ -136,11 +136,6 @@ __device__ __forceinline__ int64_t resolve_slot(const Params& p, int b, int64_t 
   return s;
 }
 
-__device__ __forceinline__ float load_elem(const void* base, int dtype, int64_t idx) {
-  if (dtype == MLA_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx]);
-  return reinterpret_cast<const float*>(base)[idx];
-}
-
 // One work item: row group g of sequence b over KV tiles [t0, t1).
 struct Item {
   int b, g, k;
