@@ -523,6 +523,23 @@ def run_ddtree(args, dev, stream, dist, with_oracle: bool):
     return res
 
 
+def run_ddtree_only(args):
+    import torch
+    from mla_tree_verify_absorbed_gb300 import api
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    api.load()
+    res = run_ddtree(args, dev, torch.cuda.current_stream(dev), dist, with_oracle=False)
+    if rank == 0:
+        print(json.dumps({"ddtree": res, "n_gpus": world, "steps": args.steps, "warmup": args.warmup}), flush=True)
+    return 0
+
+
 def run_graph(args, p, di, dev, stream, algo, dist):
     """The same call captured once in a CUDA graph and replayed K times
     (device-resident inputs): what a decode loop that captures its verify
@@ -618,11 +635,15 @@ def main(argv=None):
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--compact", action="store_true", help="also time KV compaction of the workload's rows")
     ap.add_argument("--no-ddtree", action="store_true", help="skip the DDTree construction / acceptance timing")
+    ap.add_argument("--ddtree-only", action="store_true",
+                    help="time only DDTree construction / acceptance and print that block as one JSON line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3  # timing rule: at least three untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
+    if args.ddtree_only:
+        return run_ddtree_only(args)
     return run_ours(args)
 
 
