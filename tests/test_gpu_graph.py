@@ -70,3 +70,30 @@ def test_graph_replay_matches_eager(algo):
     go, gl = PT.gather_rows(out, lse, rows)
     PT.assert_close(go, ro, "bf16", f"graph/{algo} out")
     PT.assert_close(gl, rl, "bf16", f"graph/{algo} lse")
+
+
+@pytest.mark.parametrize("algo", ["tc", "simt"])
+def test_overlapped_launches_match_plain_launches(algo):
+    # Without profiling events the metadata, attention and combine kernels
+    # are launched with programmatic stream serialization (each may start
+    # while the previous one finishes); with events they are plain launches.
+    # Both must give the same bytes, back to back on one stream, many times.
+    p = I.make_problem(name="pdl", dtype="bf16", B=3, H=16, Q=8, prefix_lens=[3000, 17, 1200], seed=81,
+                       layout="scattered", pool_slots=8192)
+    di = api.device_inputs(p)
+    ref_o, ref_l = api.verify_attn(di, algo=algo, num_splits=3)
+    evs = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    for e in evs:
+        e.record()
+    plain_o, plain_l = api.verify_attn(di, algo=algo, num_splits=3, profile_events=evs)
+    torch.cuda.synchronize()
+    assert torch.equal(plain_o, ref_o) and torch.equal(plain_l, ref_l)
+    ws = api.alloc_workspace(api.workspace_size(di, 3, algo))
+    outs = []
+    for _ in range(20):
+        o, l = api.verify_attn(di, algo=algo, num_splits=3, workspace=ws)
+        outs.append((o, l))
+    torch.cuda.synchronize()
+    assert api.check(ws) == 0
+    for o, l in outs:
+        assert torch.equal(o, ref_o) and torch.equal(l, ref_l)
