@@ -251,3 +251,21 @@ def test_ddtree_accept_argument_checks(lib, field, value):
     c = fake_accept_args(**{field: value})
     st = lib.mla_ddtree_accept(ctypes.byref(c), ctypes.c_void_p(0x100000), ctypes.c_size_t(256), None)
     assert st == api.MLA_ERR_INVALID_ARG
+
+
+def test_headers_are_plain_c(tmp_path):
+    # The boundary is a C ABI: both headers compile as C99 on their own (no
+    # CUDA or C++ headers), and every declared function can be referenced.
+    names = declared_functions()
+    src = "#include <mla_verify.h>\n#include <mla_ddtree.h>\n"
+    src += "typedef void (*mla_any_fn)(void);\n"
+    src += "mla_any_fn mla_abi_table[] = {\n" + ",\n".join(f"  (mla_any_fn)&{n}" for n in names) + "\n};\n"
+    src += "int mla_abi_sizes(void) { return (int)(sizeof(mla_verify_args) + sizeof(mla_ddtree_build_args)"
+    src += " + sizeof(mla_ddtree_accept_args)); }\n"
+    c = tmp_path / "abi.c"
+    c.write_text(src)
+    import subprocess
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-c", str(c),
+                        "-I", os.path.join(ROOT, "include"), "-o", str(tmp_path / "abi.o")],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
