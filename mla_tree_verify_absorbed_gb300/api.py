@@ -357,10 +357,72 @@ def _ws_bytes(workspace) -> int:
     return workspace.numel() * workspace.element_size()
 
 
+def _need(t, name: str, dtype, shape):
+    """The C ABI sees only a pointer: check what it cannot (dtype, shape,
+    contiguity, device) before handing it over."""
+    import torch
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _on_cuda(**tensors):
+    for name, t in tensors.items():
+        if t is not None and t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _check_build(root_token, cand_token, cand_logp, B, L, K, Q, tree_parent, tree_token, tree_depth, tree_score,
+                 workspace):
+    import torch
+    _need(cand_logp, "cand_logp", torch.float32, (B, L, K))
+    _need(cand_token, "cand_token", torch.int32, (B, L, K))
+    _need(root_token, "root_token", torch.int32, (B,))
+    for t, name in ((tree_parent, "tree_parent"), (tree_token, "tree_token")):
+        _need(t, name, torch.int32, (B, Q))
+    if tree_depth is not None:
+        _need(tree_depth, "tree_depth", torch.int32, (B, Q))
+    if tree_score is not None:
+        _need(tree_score, "tree_score", torch.float32, (B, Q))
+    _on_cuda(cand_logp=cand_logp, cand_token=cand_token, root_token=root_token, tree_parent=tree_parent,
+             tree_token=tree_token, tree_depth=tree_depth, tree_score=tree_score, workspace=workspace)
+
+
+def _check_accept(tree_parent, tree_token, target_token, accept_len, accept_nodes, next_token, node_slot,
+                  accept_slots, workspace, B, Q):
+    import torch
+    for t, name in ((tree_parent, "tree_parent"), (tree_token, "tree_token"), (target_token, "target_token"),
+                    (accept_nodes, "accept_nodes")):
+        _need(t, name, torch.int32, (B, Q))
+    for t, name in ((accept_len, "accept_len"), (next_token, "next_token")):
+        _need(t, name, torch.int32, (B,))
+    if node_slot is not None:
+        _need(node_slot, "node_slot", torch.int32, (B, Q))
+    if accept_slots is not None:
+        _need(accept_slots, "accept_slots", torch.int32, (B, Q))
+    _on_cuda(tree_parent=tree_parent, tree_token=tree_token, target_token=target_token, accept_nodes=accept_nodes,
+             accept_len=accept_len, next_token=next_token, node_slot=node_slot, accept_slots=accept_slots,
+             workspace=workspace)
+
+
 def ddtree_build_into(root_token, cand_token, cand_logp, budget: int, tree_parent, tree_token, workspace,
-                      tree_depth=None, tree_score=None, stream=None):
-    """mla_ddtree_build into caller-provided [B][budget+1] outputs (no host synchronisation)."""
+                      tree_depth=None, tree_score=None, stream=None, check: bool = True):
+    """mla_ddtree_build into caller-provided [B][budget+1] outputs (no host
+    synchronisation).  check=False skips the tensor checks, for a loop that
+    passes tensors it has already passed once with checking on."""
+    if cand_logp.dim() != 3:
+        raise ValueError("cand_logp must be [B][L][K]")
     B, L, K = cand_logp.shape
+    Q = int(budget) + 1
+    if check:
+        _check_build(root_token, cand_token, cand_logp, B, L, K, Q, tree_parent, tree_token, tree_depth, tree_score,
+                     workspace)
     a = MlaDdtreeBuildArgs()
     a.B, a.L, a.K, a.budget = B, L, K, int(budget)
     a.root_token, a.cand_token, a.cand_logp = _ptr(root_token), _ptr(cand_token), _ptr(cand_logp)
@@ -390,9 +452,15 @@ def ddtree_build(root_token, cand_token, cand_logp, budget: int, workspace=None,
 
 
 def ddtree_accept_into(tree_parent, tree_token, target_token, accept_len, accept_nodes, next_token, workspace,
-                       node_slot=None, accept_slots=None, stream=None):
-    """mla_ddtree_accept into caller-provided outputs (no host synchronisation)."""
+                       node_slot=None, accept_slots=None, stream=None, check: bool = True):
+    """mla_ddtree_accept into caller-provided outputs (no host synchronisation);
+    check as for ddtree_build_into."""
+    if tree_parent.dim() != 2:
+        raise ValueError("tree_parent must be [B][Q]")
     B, Q = tree_parent.shape
+    if check:
+        _check_accept(tree_parent, tree_token, target_token, accept_len, accept_nodes, next_token, node_slot,
+                      accept_slots, workspace, B, Q)
     a = MlaDdtreeAcceptArgs()
     a.B, a.Q = B, Q
     a.tree_parent, a.tree_token, a.target_token = _ptr(tree_parent), _ptr(tree_token), _ptr(target_token)

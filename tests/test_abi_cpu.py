@@ -269,3 +269,30 @@ def test_headers_are_plain_c(tmp_path):
                         "-I", os.path.join(ROOT, "include"), "-o", str(tmp_path / "abi.o")],
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_ddtree_binding_rejects_wrong_tensors(lib):
+    # checks the binding makes before any pointer reaches the library
+    torch = pytest.importorskip("torch")
+    ws = torch.zeros(256, dtype=torch.uint8)
+    B, L, K = 2, 4, 3
+    root = torch.zeros(B, dtype=torch.int32)
+    tok = torch.zeros(B, L, K, dtype=torch.int32)
+    lp = torch.zeros(B, L, K, dtype=torch.float32)
+    par = torch.zeros(B, 6, dtype=torch.int32)
+    tt = torch.zeros(B, 6, dtype=torch.int32)
+    with pytest.raises(ValueError, match="dtype"):
+        api.ddtree_build_into(root, tok, lp.double(), 5, par, tt, ws)
+    with pytest.raises(ValueError, match="dtype"):
+        api.ddtree_build_into(root.long(), tok, lp, 5, par, tt, ws)
+    with pytest.raises(ValueError, match="shape"):
+        api.ddtree_build_into(root, tok, lp, 4, par, tt, ws)  # outputs sized for budget 5
+    with pytest.raises(ValueError, match="contiguous"):
+        api.ddtree_build_into(root, tok.transpose(1, 2).contiguous().transpose(1, 2), lp, 5, par, tt, ws)
+    with pytest.raises(ValueError, match="CUDA"):
+        api.ddtree_build_into(root, tok, lp, 5, par, tt, ws)  # CPU tensors
+    n = torch.zeros(B, dtype=torch.int32)
+    with pytest.raises(ValueError, match="dtype"):
+        api.ddtree_accept_into(par, tt, tt.long(), n, par, n, ws)
+    with pytest.raises(ValueError, match="shape"):
+        api.ddtree_accept_into(par, tt, tt, n[:1], par, n, ws)
