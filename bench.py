@@ -322,7 +322,7 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     t_start.record(stream)
     for k in range(args.steps):
-        api.verify_attn(di, out=out, lse=lse, num_splits=args.num_splits, algo=algo, workspace=ws)
+        api.verify_attn(di, out=out, lse=lse, num_splits=args.num_splits, algo=algo, workspace=ws, check=False)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(dist)
@@ -335,7 +335,7 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     for k in range(args.steps):
         api.verify_attn(di, out=out, lse=lse, num_splits=args.num_splits, algo=algo, workspace=ws,
-                        profile_events=evs[k])
+                        profile_events=evs[k], check=False)
     torch.cuda.synchronize(dev)
     attn_ms = [a.elapsed_time(b) for a, b in evs]
     attn_avg_ms = max_over_ranks(dist, float(np.mean(attn_ms)), device=dev)
@@ -453,7 +453,7 @@ def run_compact(args, p, di, dev, stream, dist):
     torch.cuda.synchronize(dev)
     a.record(stream)
     for _ in range(args.steps):
-        api.verify_attn(dc, out=out, lse=lse, num_splits=args.num_splits, workspace=vws)
+        api.verify_attn(dc, out=out, lse=lse, num_splits=args.num_splits, workspace=vws, check=False)
     b.record(stream)
     torch.cuda.synchronize(dev)
     vms = max_over_ranks(dist, a.elapsed_time(b), device=dev) / args.steps
@@ -560,7 +560,7 @@ def run_graph(args, p, di, dev, stream, algo, dist):
     torch.cuda.synchronize(dev)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        api.verify_attn(di, out=out, lse=lse, num_splits=args.num_splits, algo=algo, workspace=ws)
+        api.verify_attn(di, out=out, lse=lse, num_splits=args.num_splits, algo=algo, workspace=ws, check=False)
     for _ in range(max(1, args.warmup)):
         g.replay()
     torch.cuda.synchronize(dev)
@@ -601,7 +601,7 @@ def run_e2e(args, p, di, dev, stream, algo, dist):
     def step():
         for name, h in host.items():
             getattr(di, name).copy_(h, non_blocking=True)
-        api.verify_attn(di, out=out, lse=lse, num_splits=args.num_splits, algo=algo, workspace=ws)
+        api.verify_attn(di, out=out, lse=lse, num_splits=args.num_splits, algo=algo, workspace=ws, check=False)
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
 

@@ -159,6 +159,40 @@ class DeviceInputs:
     def pool_slots(self) -> int:
         return int(self.kv_c.shape[0])
 
+    def check(self):
+        """What the C ABI cannot see from pointers: element types, shapes,
+        layouts and the device of every tensor.  Raises ValueError."""
+        self.check_layout()
+        _on_cuda(**self.tensors())
+
+    def tensors(self):
+        return dict(q_lat=self.q_lat, q_pe=self.q_pe, kv_c=self.kv_c, k_pe=self.k_pe, prefix_lens=self.prefix_lens,
+                    tree_parent=self.tree_parent, kv_indptr=self.kv_indptr, kv_indices=self.kv_indices,
+                    block_table=self.block_table)
+
+    def check_layout(self):
+        import torch
+        el = torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        B, Q, H = self.B, self.Q, self.H
+        _need(self.q_lat, "q_lat", el, (B, Q, H, 512))
+        _need(self.q_pe, "q_pe", el, (B, Q, H, 64))
+        for t, name, w in ((self.kv_c, "kv_c", 512), (self.k_pe, "k_pe", 64)):
+            if t is None or t.dtype != el or t.dim() != 2 or t.shape[1] != w or t.stride(1) != 1:
+                raise ValueError(f"{name} must be a [slots][{w}] {el} view with unit column stride")
+        if self.k_pe.shape[0] != self.kv_c.shape[0]:
+            raise ValueError("kv_c and k_pe must cover the same pool slots")
+        _need(self.prefix_lens, "prefix_lens", torch.int32, (B,))
+        _need(self.tree_parent, "tree_parent", torch.int32, (B, Q))
+        if self.page_size == 1:
+            _need(self.kv_indptr, "kv_indptr", torch.int32, (B + 1,))
+            if self.kv_indices is None or self.kv_indices.dtype != torch.int32 or self.kv_indices.dim() != 1 \
+                    or not self.kv_indices.is_contiguous():
+                raise ValueError("kv_indices must be a contiguous 1-D int32 tensor")
+        else:
+            if self.block_table is None or self.block_table.dtype != torch.int32 or self.block_table.dim() != 2 \
+                    or self.block_table.shape[0] != B or not self.block_table.is_contiguous():
+                raise ValueError("block_table must be a contiguous [B][max_pages] int32 tensor")
+
 
 def device_inputs(problem, device="cuda", separate_pools: bool = False) -> DeviceInputs:
     """Copy a numpy inputs.Problem to the device (packed [slot][576] pool by
@@ -192,7 +226,16 @@ def device_inputs(problem, device="cuda", separate_pools: bool = False) -> Devic
 
 
 def make_args(di: DeviceInputs, out=None, lse=None, algo: str = "auto",
-              profile_events=None) -> MlaVerifyArgs:
+              profile_events=None, check: bool = True) -> MlaVerifyArgs:
+    if check:
+        import torch
+        di.check_layout()
+        odt = torch.bfloat16 if di.dtype == "bf16" else torch.float32
+        if out is not None:
+            _need(out, "out", odt, (di.B, di.Q, di.H, 512))
+        if lse is not None:
+            _need(lse, "lse", torch.float32, (di.B, di.Q, di.H))
+        _on_cuda(out=out, lse=lse, **di.tensors())
     a = MlaVerifyArgs()
     a.B, a.Q, a.H = di.B, di.Q, di.H
     a.dtype = MLA_BF16 if di.dtype == "bf16" else MLA_FP32
@@ -217,7 +260,7 @@ def make_args(di: DeviceInputs, out=None, lse=None, algo: str = "auto",
 
 
 def workspace_size(di: DeviceInputs, num_splits: int = 0, algo: str = "auto") -> int:
-    a = make_args(di, algo=algo)
+    a = make_args(di, algo=algo, check=False)
     n = load().mla_verify_workspace_size(ctypes.byref(a), int(num_splits))
     if n == 0 and di.B > 0 and di.Q > 0:
         raise MlaError(MLA_ERR_INVALID_ARG, "mla_verify_workspace_size")
@@ -237,8 +280,9 @@ def alloc_workspace(nbytes: int, device="cuda"):
 
 
 def verify_attn(di: DeviceInputs, out=None, lse=None, num_splits: int = 0, algo: str = "auto",
-                workspace=None, stream=None, profile_events=None):
-    """Run mla_verify_attn; returns (out [B,Q,H,512], lse [B,Q,H] fp32)."""
+                workspace=None, stream=None, profile_events=None, check: bool = True):
+    """Run mla_verify_attn; returns (out [B,Q,H,512], lse [B,Q,H] fp32).
+    check=False skips the tensor checks (a loop that already passed them)."""
     import torch
     dev = di.q_lat.device
     odt = torch.bfloat16 if di.dtype == "bf16" else torch.float32
@@ -246,7 +290,7 @@ def verify_attn(di: DeviceInputs, out=None, lse=None, num_splits: int = 0, algo:
         out = torch.empty((di.B, di.Q, di.H, 512), dtype=odt, device=dev)
     if lse is None:
         lse = torch.empty((di.B, di.Q, di.H), dtype=torch.float32, device=dev)
-    a = make_args(di, out, lse, algo, profile_events)
+    a = make_args(di, out, lse, algo, profile_events, check)
     lib = load()
     need = lib.mla_verify_workspace_size(ctypes.byref(a), int(num_splits))
     if workspace is None:

@@ -296,3 +296,24 @@ def test_ddtree_binding_rejects_wrong_tensors(lib):
         api.ddtree_accept_into(par, tt, tt.long(), n, par, n, ws)
     with pytest.raises(ValueError, match="shape"):
         api.ddtree_accept_into(par, tt, tt, n[:1], par, n, ws)
+
+
+def test_device_inputs_check_catches_wrong_tensors():
+    torch = pytest.importorskip("torch")
+    import dataclasses
+    from mla_tree_verify_absorbed_gb300 import inputs as I
+    p = I.make_problem(name="chk", dtype="bf16", B=2, H=4, Q=3, prefix_lens=[5, 9], seed=1,
+                       layout="scattered", pool_slots=64)
+    di = api.device_inputs(p, device="cpu")
+    with pytest.raises(ValueError, match="CUDA"):
+        di.check()  # everything right but the device
+    with pytest.raises(ValueError, match="prefix_lens"):
+        dataclasses.replace(di, prefix_lens=di.prefix_lens.long()).check()
+    with pytest.raises(ValueError, match="q_lat"):
+        dataclasses.replace(di, q_lat=di.q_lat.float()).check()
+    with pytest.raises(ValueError, match="kv_c"):
+        dataclasses.replace(di, kv_c=di.pool[:, :256]).check()
+    with pytest.raises(ValueError, match="kv_indices"):
+        dataclasses.replace(di, kv_indices=di.kv_indices.long()).check()
+    with pytest.raises(ValueError, match="out"):
+        api.make_args(di, out=torch.zeros(2, 3, 4, 256, dtype=torch.bfloat16))
