@@ -267,7 +267,8 @@ def run_reference(args):
     total_rows = p.B * p.H * p.Q
     us_call = float(np.mean(times)) * total_rows * 1e6
     line = {
-        "impl": "reference", "metric": METRIC, "value": us_call, "unit": UNIT, "n_gpus": 0,
+        "impl": "reference", "metric": METRIC, "value": us_call, "unit": UNIT, "n_gpus": world,
+        "device": "host cores (the oracle uses no GPU)",
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": us_call / 1000.0,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": f"{args.workload}: {workload_desc(args.workload, p)}"},
