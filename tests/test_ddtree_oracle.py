@@ -69,3 +69,24 @@ def test_mutant_is_caught(name, tmp_path):
         return  # a mutant that never finishes is caught too
     failed = [l for l in r.stdout.splitlines() if l.startswith("FAILED:")]
     assert r.returncode != 0 or (failed and failed[0] != "FAILED:"), r.stdout + r.stderr
+
+
+def test_oracle_equals_brute_force_on_random_tiny_drafts():
+    hyp = pytest.importorskip("hypothesis")
+    st = hyp.strategies
+    import numpy as np
+
+    values = [0.0, -0.25, -0.5, -1.0, -3.0, float("-inf")]
+
+    @hyp.settings(max_examples=300, deadline=None)
+    @hyp.given(L=st.integers(1, 4), K=st.integers(1, 3), data=st.data())
+    def check(L, K, data):
+        lp = np.array([sorted(data.draw(st.lists(st.sampled_from(values), min_size=K, max_size=K)), reverse=True)
+                       for _ in range(L)], dtype=np.float32)
+        tok = np.arange(L * K, dtype=np.int32).reshape(L, K) + 100
+        budget = data.draw(st.integers(1, ddtree.node_count(L, K)))
+        got = ddtree.build_tree_one(7, tok, lp, budget)
+        want = pins._brute(7, tok, lp, budget)
+        assert got[0].tolist() == want[0] and got[1].tolist() == want[1] and got[2].tolist() == want[2]
+
+    check()
