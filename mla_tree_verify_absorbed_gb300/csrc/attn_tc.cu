@@ -56,6 +56,8 @@
 // Every wait is bounded; on timeout the kernel raises an abort flag in all
 // four CTAs, sets MLA_DEVERR_TIMEOUT, stops issuing work, drains the MMAs it
 // issued, frees TMEM and returns.
+#include <mutex>
+
 #include "common.cuh"
 #include "sm100.cuh"
 
@@ -801,10 +803,21 @@ int tc_rows_per_group() { return tc::kRG; }
 int tc_tokens_per_tile() { return tc::kTK; }
 int tc_default_for(int dtype) { return dtype == MLA_BF16 ? MLA_ALGO_TC : MLA_ALGO_SIMT; }
 
-// Clusters of four CTAs that can be resident at once (one CTA per SM).
+// Clusters of four CTAs that can be resident at once on the current device
+// (one CTA per SM), looked up once per device under a lock, so a process
+// that drives GPUs of different kinds, or calls from several threads, gets
+// each device's own figure.
 int tc_clusters_per_gpu(int sm_count) {
-  static int cached = -1;
-  if (cached > 0) return cached;
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static int cached[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return sm_count / tc::kClusterCtas;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] > 0) return cached[dev];
   cudaFuncSetAttribute(tc::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemAlloc);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tc::kClusterCtas * (sm_count / tc::kClusterCtas), 1, 1);
@@ -815,7 +828,7 @@ int tc_clusters_per_gpu(int sm_count) {
     cudaGetLastError();
     n = sm_count / tc::kClusterCtas;
   }
-  cached = n;
+  cached[dev] = n;
   return n;
 }
 
