@@ -164,6 +164,8 @@ int oracle_verify_rows(const oracle_problem *pr, int n_rows, const int32_t *rows
         for (int d = 0; d < ORACLE_DL; ++d)
             o[d] = 0.0;
         if (b < 0 || b >= B || i < 0 || i >= Q || h < 0 || h >= H) {
+            /* written by several threads, only ever to 1 */
+#pragma omp atomic write
             bad = 1;
             continue;
         }
@@ -180,6 +182,8 @@ int oracle_verify_rows(const oracle_problem *pr, int n_rows, const int32_t *rows
         if (!pos || !s) {
             free(pos);
             free(s);
+            /* written by several threads, only ever to 1 */
+#pragma omp atomic write
             bad = 1;
             continue;
         }
@@ -210,6 +214,8 @@ int oracle_verify_rows(const oracle_problem *pr, int n_rows, const int32_t *rows
             s[j] = pr->scale * (dot_lat + dot_pe);
         }
         if (row_bad) {
+            /* written by several threads, only ever to 1 */
+#pragma omp atomic write
             bad = 1;
             free(pos);
             free(s);
