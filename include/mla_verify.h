@@ -138,18 +138,33 @@ mla_status mla_verify_attn(const mla_verify_args *args, void *workspace, size_t 
  * synchronisation of cudaMalloc) and so have no workspace to pass.  The pages
  * have no counterpart of this entry point.
  * It allocates nothing: its workspace is a fixed array of
- * MLA_NOALLOC_SCRATCH_BYTES compiled into the library, held on every device
- * that loads the library until the process exits.  Arguments, outputs and
- * num_splits mean what they mean for mla_verify_attn; a call whose
- * mla_verify_workspace_size exceeds MLA_NOALLOC_SCRATCH_BYTES returns
- * MLA_ERR_WORKSPACE before launching anything (use fewer splits, or
- * mla_verify_attn).  The first call on a device looks up the array's device
- * address and caches it; make that first call before any stream capture.
- * All calls share the array and it keeps the previous call's contents (the
- * error word is cleared at the start of each call); calls that overlap on the
- * GPU race on it, so order them on one stream. */
+ * MLA_NOALLOC_SCRATCH_BYTES compiled into the library.  The array is reserved
+ * on a device when the library's device code is loaded there, which under
+ * lazy module loading (the CUDA default) happens during the first call on that
+ * device: make that first call at start-up, before an engine claims the rest
+ * of the device memory and before any stream capture.  It stays reserved until
+ * the process exits.  Arguments and outputs mean what they mean for
+ * mla_verify_attn.  num_splits > 0: that many KV chunks per row group; a call
+ * whose mla_verify_workspace_size exceeds MLA_NOALLOC_SCRATCH_BYTES returns
+ * MLA_ERR_WORKSPACE before launching anything.  num_splits == 0: the automatic
+ * split count, lowered until the workspace fits the array (one split always
+ * fits), so the results can differ in fp32 rounding from mla_verify_attn's
+ * automatic choice on large problems.  The device address of the array is
+ * looked up once per CUDA context (a context created after cudaDeviceReset is
+ * looked up again).  All calls share the array and it keeps the previous
+ * call's contents (the error word is cleared at the start of each call); calls
+ * that overlap on the GPU race on it, so order them on one stream.  Device-side
+ * table errors are reported in the array's error word: read it with
+ * mla_verify_noalloc_check. */
 #define MLA_NOALLOC_SCRATCH_BYTES (32u << 20)
 mla_status mla_verify_attn_noalloc(const mla_verify_args *args, int num_splits, mla_stream_t stream);
+
+/* mla_verify_check for mla_verify_attn_noalloc: synchronises `stream`, then
+ * reads the error word the last no-allocation call on the current device left
+ * in the library's scratch array.  Returns MLA_OK or MLA_ERR_DEVICE_CHECK (or
+ * MLA_ERR_CUDA); *bits (may be NULL) receives the raw MLA_DEVERR_* bits.
+ * Allocates nothing.  No counterpart on the pages. */
+mla_status mla_verify_noalloc_check(mla_stream_t stream, uint32_t *bits);
 
 /* Parity / debug export of the index work the attention kernels rely on.
  * Runs the metadata kernel and writes

@@ -27,7 +27,7 @@ DEVERR = {
 }
 
 # every symbol include/*.h declares
-EXPORTS = ("mla_verify_workspace_size", "mla_verify_attn", "mla_verify_attn_noalloc",
+EXPORTS = ("mla_verify_workspace_size", "mla_verify_attn", "mla_verify_attn_noalloc", "mla_verify_noalloc_check",
            "mla_verify_build_meta", "mla_verify_check", "mla_status_str", "mla_verify_abi_version",
            "mla_verify_selftest_timeout", "mla_kv_compact", "mla_ddtree_build", "mla_ddtree_accept")
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -97,6 +97,8 @@ def load(path: Optional[str] = None):
                                     ctypes.c_int, ctypes.c_void_p]
     lib.mla_verify_attn_noalloc.restype = ctypes.c_int
     lib.mla_verify_attn_noalloc.argtypes = [ctypes.POINTER(MlaVerifyArgs), ctypes.c_int, ctypes.c_void_p]
+    lib.mla_verify_noalloc_check.restype = ctypes.c_int
+    lib.mla_verify_noalloc_check.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
     lib.mla_verify_build_meta.restype = ctypes.c_int
     lib.mla_verify_build_meta.argtypes = [ctypes.POINTER(MlaVerifyArgs), ctypes.c_void_p, ctypes.c_size_t,
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
@@ -304,10 +306,12 @@ def verify_attn(di: DeviceInputs, out=None, lse=None, num_splits: int = 0, algo:
 
 
 def verify_attn_noalloc(di: DeviceInputs, out=None, lse=None, num_splits: int = 0, algo: str = "auto",
-                        stream=None):
+                        stream=None, check_device: bool = False):
     """Run mla_verify_attn_noalloc (library-held scratch, no workspace); returns
     (out, lse).  Output tensors are created here when not given -- the library
-    call itself allocates nothing."""
+    call itself allocates nothing.  check_device=True synchronises the stream
+    and raises MlaError(MLA_ERR_DEVICE_CHECK) when the device found bad table
+    contents (noalloc_check)."""
     import torch
     dev = di.q_lat.device
     odt = torch.bfloat16 if di.dtype == "bf16" else torch.float32
@@ -319,7 +323,19 @@ def verify_attn_noalloc(di: DeviceInputs, out=None, lse=None, num_splits: int = 
     st = load().mla_verify_attn_noalloc(ctypes.byref(a), int(num_splits), _stream(stream))
     if st != MLA_OK:
         raise MlaError(st, "mla_verify_attn_noalloc")
+    if check_device and noalloc_check(stream) != 0:
+        raise MlaError(MLA_ERR_DEVICE_CHECK, "mla_verify_attn_noalloc")
     return out, lse
+
+
+def noalloc_check(stream=None) -> int:
+    """Synchronise and return the device error bits the last
+    mla_verify_attn_noalloc call on the current device left."""
+    bits = ctypes.c_uint32(0)
+    st = load().mla_verify_noalloc_check(_stream(stream), ctypes.byref(bits))
+    if st not in (MLA_OK, MLA_ERR_DEVICE_CHECK):
+        raise MlaError(st, "mla_verify_noalloc_check")
+    return int(bits.value)
 
 
 def selftest_timeout(di: DeviceInputs, out, lse, workspace, hold_ns: int, stream=None):

@@ -206,6 +206,16 @@ mla_status check_ws(const Plan& pl, const void* ws, size_t ws_bytes) {
 
 }  // namespace
 
+namespace mlav {
+// The split count a call with these arguments and num_splits would use
+// (num_splits itself when > 0), or -1 when the arguments are invalid.
+int plan_splits(const mla_verify_args* a, int num_splits) {
+  Plan pl;
+  if (make_plan(a, num_splits, &pl) != MLA_OK) return -1;
+  return pl.noop ? 1 : pl.splits;
+}
+}  // namespace mlav
+
 extern "C" {
 
 size_t mla_verify_workspace_size(const mla_verify_args* a, int num_splits) {
