@@ -5,6 +5,7 @@ oracle results.  The tolerance for bf16 caches is max|d| <= 1e-2 * max|ref| +
 from __future__ import annotations
 
 import functools
+import os
 
 import numpy as np
 
@@ -25,8 +26,17 @@ def tol_ok(got: np.ndarray, ref: np.ndarray, dtype: str):
     return dmax <= bound, dmax, bound, mx
 
 
+# Achieved margins of every comparison in this session: (test, what, max|d|,
+# max|ref|, bound).  conftest.py writes them out when MLA_PARITY_MARGINS
+# names a file.
+MARGINS = []
+
+
 def assert_close(got, ref, dtype, what=""):
     ok, dmax, bound, mx = tol_ok(got, ref, dtype)
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    MARGINS.append(dict(test=test, what=what, dtype=dtype, max_abs_diff=dmax, max_abs_ref=mx, bound=bound,
+                        rel=dmax / max(mx, 1e-30), passed=bool(ok)))
     assert ok, f"{what}: max|d|={dmax:.3e} > bound {bound:.3e} (max|ref|={mx:.3e})"
     return dmax / max(mx, 1e-30)
 

@@ -156,6 +156,23 @@ def test_edge_trees(algo):
 # full-size workloads, in the launch configuration the benchmark times
 # (num_splits = 0, default kernel family): sampled rows against the oracle
 # ---------------------------------------------------------------------------
+def test_lse_single_needle_c3():
+    # one planted token that every row of the 200k-prefix workload sees: its
+    # weight dominates every row's normaliser (score ~35 against ln Z ~14 for
+    # the other 200k tokens), so a wrong gather of that one slot, or a wrong
+    # scale on it, moves lse by several units -- far above the tolerance --
+    # and the recorded margin shows how close the kernel really is
+    p = I.make_config("c3")
+    I.plant_needles(p, seed=7, n_prefix=1, strength=60.0)
+    _, out, lse = run(p)
+    rows = I.sample_rows(p, 2, seed=33)
+    ro, rl = PT.oracle_rows(p, rows)
+    go, gl = PT.gather_rows(out, lse, rows)
+    assert rl.min() > 18.0, rl.min()  # the needle dominates every sampled row
+    PT.assert_close(go, ro, "bf16", "c3 single-needle out")
+    PT.assert_close(gl, rl, "bf16", "c3 single-needle lse")
+
+
 @pytest.mark.parametrize("name,heads,needles", [
     ("c2", 8, False), ("c2", 4, True), ("c3", 2, False), ("c3", 2, True),
     ("c4", 2, False), ("c5", 2, False), ("c6", 8, False), ("c6", 8, True),
