@@ -341,6 +341,18 @@ def run_ours(args):
     attn_ms = [a.elapsed_time(b) for a, b in evs]
     attn_avg_ms = max_over_ranks(dist, float(np.mean(attn_ms)), device=dev)
 
+    # --- the same calls with L2 flushed between them --------------------------
+    l2_flushed = None
+    if not args.no_l2_flush:
+        flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
+        f_steps = max(10, min(args.steps, 20))
+        f_call, f_kernel = time_calls(di, p, dev, stream, dist, f_steps, args.warmup, algo, args.num_splits, flush)
+        l2_flushed = {"us_per_call": job_us_per_call(f_call, world), "kernel_us": f_kernel * 1000.0,
+                      "steps": f_steps, "flush_bytes": L2_FLUSH_BYTES,
+                      "note": "a buffer larger than L2 written between calls, outside the timed events"}
+        del flush
+        torch.cuda.empty_cache()
+
     # --- end to end through the public API with host buffers ----------------
     e2e = None
     if not args.no_e2e:
@@ -349,8 +361,11 @@ def run_ours(args):
     if not args.no_graph:
         graph = run_graph(args, p, di, dev, stream, algo, dist)
     compact = None
-    if args.compact:
+    if not args.no_compact:
         compact = run_compact(args, p, di, dev, stream, dist)
+    workloads = None
+    if not args.no_workloads:
+        workloads = run_workloads(args, dev, stream, dist, world)
     ddtree = None
     if not args.no_ddtree:
         ddtree = run_ddtree(args, dev, stream, dist, with_oracle=(world == 1 and not args.no_cpu_baseline))
@@ -404,14 +419,108 @@ def run_ours(args):
         line["e2e"] = e2e
     if graph is not None:
         line["graph"] = graph
+    if l2_flushed is not None:
+        line["l2_flushed"] = l2_flushed
     if compact is not None:
         line["kv_compact"] = compact
+    if workloads is not None:
+        line["workloads"] = workloads
     if ddtree is not None:
         line["ddtree"] = ddtree
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p)
     print(json.dumps(line), flush=True)
     return 0
+
+
+L2_FLUSH_BYTES = 512 << 20  # written between calls of the L2-flushed timing: about four times the L2
+
+
+def time_calls(di, p, dev, stream, dist, steps, warmup, algo="auto", num_splits=0, flush=None):
+    """Device-resident timing of `steps` verify calls of one workload:
+    per-call time (events around the back-to-back loop; with `flush`, events
+    around each call and a buffer larger than L2 written between calls,
+    outside the events) and the attention kernel alone (the call's
+    profiling events)."""
+    import torch
+    from mla_tree_verify_absorbed_gb300 import api
+
+    out = torch.empty((p.B, p.Q, p.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((p.B, p.Q, p.H), dtype=torch.float32, device=dev)
+    ws = api.alloc_workspace(api.workspace_size(di, num_splits, algo), dev)
+    for _ in range(max(3, warmup)):
+        api.verify_attn(di, out=out, lse=lse, num_splits=num_splits, algo=algo, workspace=ws)
+    torch.cuda.synchronize(dev)
+    if api.check(ws):
+        raise RuntimeError(f"{p.name}: device table check failed")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        a.record(stream)
+        b.record(stream)
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    if flush is None:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            api.verify_attn(di, out=out, lse=lse, num_splits=num_splits, algo=algo, workspace=ws, check=False)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        call_ms = a.elapsed_time(b) / steps
+    else:
+        calls = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for k in range(steps):
+            flush.zero_()
+            calls[k][0].record(stream)
+            api.verify_attn(di, out=out, lse=lse, num_splits=num_splits, algo=algo, workspace=ws, check=False)
+            calls[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        call_ms = float(np.mean([x.elapsed_time(y) for x, y in calls]))
+    barrier(dist)
+    for k in range(steps):
+        if flush is not None:
+            flush.zero_()
+        api.verify_attn(di, out=out, lse=lse, num_splits=num_splits, algo=algo, workspace=ws,
+                        profile_events=evs[k], check=False)
+    torch.cuda.synchronize(dev)
+    kernel_ms = float(np.mean([x.elapsed_time(y) for x, y in evs]))
+    return max_over_ranks(dist, call_ms, device=dev), max_over_ranks(dist, kernel_ms, device=dev)
+
+
+def roofline_entry(p, call_ms, kernel_ms, world=1):
+    cnt = workload_counts(p)
+    peak, src = peak_bf16_tflops()
+    achieved = cnt["flops"] / (kernel_ms / 1000.0) / 1e12
+    return {"us_per_call": job_us_per_call(call_ms, world), "kernel_us": kernel_ms * 1000.0,
+            "gflop": cnt["flops"] / 1e9, "kv_mb": cnt["kv_bytes"] / 1e6,
+            "kernel_tflops": achieved, "frac": achieved / peak, "peak_source": f"bf16 dense, {src}",
+            "effective_kv_gbs": cnt["kv_bytes"] / (call_ms / 1000.0) / 1e9}
+
+
+def run_workloads(args, dev, stream, dist, world):
+    """Short timing blocks of the other workloads (device-resident inputs):
+    c6 (4-node chain over 200k, the small-Q regime), c2, c4 (ragged batch),
+    c5 (128 heads, paged), and the L2-flushed variant of c2."""
+    import torch
+    from mla_tree_verify_absorbed_gb300 import api
+
+    res = {}
+    steps = max(10, min(args.steps, 20))
+    flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
+    for name in ("c6", "c2", "c4", "c5"):
+        p = I.make_config(name)
+        di = api.device_inputs(p, device=dev)
+        call_ms, kernel_ms = time_calls(di, p, dev, stream, dist, steps, args.warmup)
+        entry = roofline_entry(p, call_ms, kernel_ms, world)
+        entry.update(workload=workload_desc(name, p), steps=steps)
+        if name == "c2":
+            f_call, f_kernel = time_calls(di, p, dev, stream, dist, steps, args.warmup, flush=flush)
+            entry["l2_flushed"] = {"us_per_call": f_call * 1000.0, "kernel_us": f_kernel * 1000.0,
+                                   "flush_bytes": L2_FLUSH_BYTES}
+        res[name] = entry
+        del di
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_compact(args, p, di, dev, stream, dist):
@@ -426,19 +535,20 @@ def run_compact(args, p, di, dev, stream, dist):
     new_idx = torch.empty((total,), dtype=torch.int32, device=dev)
     new_indptr = torch.empty((p.B + 1,), dtype=torch.int32, device=dev)
     ws = api.alloc_workspace(api.workspace_size(di, 1), dev)
+    steps = max(10, min(args.steps, 50))
     for _ in range(max(1, args.warmup)):
         api.kv_compact_into(di, dst, new_idx, new_indptr, ws)
     torch.cuda.synchronize(dev)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist)
     a.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         api.kv_compact_into(di, dst, new_idx, new_indptr, ws)
     b.record(stream)
     torch.cuda.synchronize(dev)
     if api.check(ws) != 0:
         raise RuntimeError("kv compaction reported a device error")
-    ms = max_over_ranks(dist, a.elapsed_time(b), device=dev) / args.steps
+    ms = max_over_ranks(dist, a.elapsed_time(b), device=dev) / steps
     moved = 2.0 * total * 576 * 2
     hbm_peak, src = peak_hbm_gbs()
     gbs = moved / (ms / 1000.0) / 1e9
@@ -453,14 +563,21 @@ def run_compact(args, p, di, dev, stream, dist):
         api.verify_attn(dc, out=out, lse=lse, num_splits=args.num_splits, workspace=vws)
     torch.cuda.synchronize(dev)
     a.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         api.verify_attn(dc, out=out, lse=lse, num_splits=args.num_splits, workspace=vws, check=False)
     b.record(stream)
     torch.cuda.synchronize(dev)
-    vms = max_over_ranks(dist, a.elapsed_time(b), device=dev) / args.steps
+    vms = max_over_ranks(dist, a.elapsed_time(b), device=dev) / steps
+    # and on the scattered layout, timed the same way in the same block
+    a.record(stream)
+    for _ in range(steps):
+        api.verify_attn(di, out=out, lse=lse, num_splits=args.num_splits, workspace=vws, check=False)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    sms = max_over_ranks(dist, a.elapsed_time(b), device=dev) / steps
     return {"us_per_call": ms * 1000.0, "rows": total, "bytes_moved": moved, "gbs": gbs,
-            "hbm_frac": gbs / hbm_peak, "hbm_peak_source": src,
-            "verify_us_on_compacted": vms * 1000.0}
+            "hbm_frac": gbs / hbm_peak, "hbm_peak_source": src, "steps": steps,
+            "verify_us_on_compacted": vms * 1000.0, "verify_us_on_scattered": sms * 1000.0}
 
 
 def run_ddtree(args, dev, stream, dist, with_oracle: bool):
@@ -624,9 +741,23 @@ def run_e2e(args, p, di, dev, stream, algo, dist):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
+def relaunch(n: int, argv) -> int:
+    """Run this script as n local processes (one replica per GPU) under
+    torch.distributed.run, rendezvous on 127.0.0.1; rank 0 prints the line."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd, cwd=ROOT)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=None,
+                    help="GPUs (one replica each); without a launcher's WORLD_SIZE, N > 1 relaunches "
+                         "this script under torch.distributed.run with N local processes")
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -636,11 +767,18 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
-    ap.add_argument("--compact", action="store_true", help="also time KV compaction of the workload's rows")
+    ap.add_argument("--no-compact", action="store_true", help="skip the KV compaction timing")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the short blocks of the other workloads")
+    ap.add_argument("--no-l2-flush", action="store_true", help="skip the L2-flushed timing")
     ap.add_argument("--no-ddtree", action="store_true", help="skip the DDTree construction / acceptance timing")
     ap.add_argument("--ddtree-only", action="store_true",
                     help="time only DDTree construction / acceptance and print that block as one JSON line")
     args = ap.parse_args(argv)
+    env_world = os.environ.get("WORLD_SIZE")
+    if env_world is None and args.gpus is not None and args.gpus > 1:
+        return relaunch(args.gpus, sys.argv[1:] if argv is None else list(argv))
+    if env_world is not None and args.gpus is not None and args.gpus != int(env_world):
+        raise SystemExit(f"--gpus {args.gpus} disagrees with the launcher's WORLD_SIZE={env_world}")
     if args.warmup < 3:
         args.warmup = 3  # timing rule: at least three untimed warm-up steps
     if args.impl == "reference":

@@ -62,3 +62,24 @@ def test_reference_arm_prints_only_on_rank_zero():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1"],
                        capture_output=True, text=True, env=env, cwd=ROOT, timeout=300)
     assert r.returncode == 0 and r.stdout.strip() == "", r.stdout + r.stderr
+
+
+def test_gpus_flag_without_launcher_spawns_one_process_per_replica():
+    # `bench.py --gpus 2` with no WORLD_SIZE relaunches itself as two local
+    # processes; the reference arm needs no GPU, and only rank 0 prints
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--workload", "tiny", "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, env=env, cwd=ROOT, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    lines = [x for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+
+
+def test_gpus_flag_must_match_the_launcher():
+    env = dict(os.environ, RANK="0", WORLD_SIZE="2", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "4",
+                        "--steps", "1"], capture_output=True, text=True, env=env, cwd=ROOT, timeout=300)
+    assert r.returncode != 0 and "disagrees" in (r.stdout + r.stderr)
