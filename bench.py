@@ -308,6 +308,7 @@ def run_ours(args):
     bits = api.check(ws)
     if bits:
         raise SystemExit(f"device table check failed: {bits:#x}")
+    splits_used = api.splits_used(ws)
 
     # --- device-resident timed region ---------------------------------------
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -403,7 +404,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {workload_desc(args.workload, p)}", "algo": resolved,
-                   "num_splits": args.num_splits,
+                   "num_splits": args.num_splits, "splits_used": splits_used,
                    "l2": "inputs larger than L2: 230 MB of KV read per call (129 MB L2)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "effective_kv_gbs": eff_kv_gbs,
@@ -436,12 +437,13 @@ def run_ours(args):
 L2_FLUSH_BYTES = 512 << 20  # written between calls of the L2-flushed timing: about four times the L2
 
 
-def time_calls(di, p, dev, stream, dist, steps, warmup, algo="auto", num_splits=0, flush=None):
+def time_calls(di, p, dev, stream, dist, steps, warmup, algo="auto", num_splits=0, flush=None, info=None):
     """Device-resident timing of `steps` verify calls of one workload:
     per-call time (events around the back-to-back loop; with `flush`, events
     around each call and a buffer larger than L2 written between calls,
     outside the events) and the attention kernel alone (the call's
-    profiling events)."""
+    profiling events).  `info`, when given, receives the split count the
+    calls used ("splits_used")."""
     import torch
     from mla_tree_verify_absorbed_gb300 import api
 
@@ -453,6 +455,8 @@ def time_calls(di, p, dev, stream, dist, steps, warmup, algo="auto", num_splits=
     torch.cuda.synchronize(dev)
     if api.check(ws):
         raise RuntimeError(f"{p.name}: device table check failed")
+    if info is not None:
+        info["splits_used"] = api.splits_used(ws)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for a, b in evs:
         a.record(stream)
@@ -510,9 +514,10 @@ def run_workloads(args, dev, stream, dist, world):
     for name in ("c6", "c2", "c4", "c5"):
         p = I.make_config(name)
         di = api.device_inputs(p, device=dev)
-        call_ms, kernel_ms = time_calls(di, p, dev, stream, dist, steps, args.warmup)
+        info = {}
+        call_ms, kernel_ms = time_calls(di, p, dev, stream, dist, steps, args.warmup, info=info)
         entry = roofline_entry(p, call_ms, kernel_ms, world)
-        entry.update(workload=workload_desc(name, p), steps=steps)
+        entry.update(workload=workload_desc(name, p), steps=steps, splits_used=info["splits_used"])
         if name == "c2":
             f_call, f_kernel = time_calls(di, p, dev, stream, dist, steps, args.warmup, flush=flush)
             entry["l2_flushed"] = {"us_per_call": f_call * 1000.0, "kernel_us": f_kernel * 1000.0,

@@ -124,11 +124,19 @@ size_t mla_verify_workspace_size(const mla_verify_args *args, int num_splits);
  * `stream`.  workspace: device memory of at least
  * mla_verify_workspace_size(args, num_splits) bytes, 256-byte aligned, not
  * used concurrently by another call.  num_splits: n > 0 cuts the KV range
- * of every row group (128 query rows for the tensor-core kernel, 16 for the
+ * of every row group (256 query rows for the tensor-core kernel, 16 for the
  * SIMT kernel) into exactly n chunks, merged by the LSE-combine kernel when
- * n > 1 (a chunk is empty when a sequence has fewer than n KV tiles); 0 picks
- * n from B, H, Q and the SM count so the work items fill the GPU in whole
- * waves.  Results do not depend on num_splits beyond fp32 rounding. */
+ * n > 1 (a chunk is empty when a sequence has fewer than n KV tiles).  0: the
+ * library chooses.  From B, H, Q and the SM count it takes S_max, the count
+ * whose work items fill the GPU in whole waves, and sizes the workspace for
+ * it; the SIMT kernel uses S_max, while for the tensor-core kernel the
+ * metadata kernel, once it has read prefix_lens, picks the count in
+ * [1, S_max] that a cost model of the kernels (time per tile and per work
+ * item, the combine's pass over the partials) rates fastest -- so the count
+ * follows the sequences' lengths without a host synchronisation, and equal
+ * inputs always get the same count (read it back with
+ * mla_verify_splits_used).  Results do not depend on the split count beyond
+ * fp32 rounding. */
 mla_status mla_verify_attn(const mla_verify_args *args, void *workspace, size_t ws_bytes,
                            int num_splits, mla_stream_t stream);
 
@@ -182,6 +190,12 @@ mla_status mla_verify_build_meta(const mla_verify_args *args, void *workspace, s
  * call that used this workspace.  Returns MLA_OK or MLA_ERR_DEVICE_CHECK (or
  * MLA_ERR_CUDA); *bits (may be NULL) receives the raw MLA_DEVERR_* bits. */
 mla_status mla_verify_check(const void *workspace, mla_stream_t stream, uint32_t *bits);
+
+/* Synchronises `stream`, then reads the split count (KV chunks per row group)
+ * that the last mla_verify_attn call on this workspace used: num_splits when
+ * that was > 0, else the one the library chose.  Debug and benchmark aid; no
+ * counterpart on the pages. */
+mla_status mla_verify_splits_used(const void *workspace, mla_stream_t stream, int32_t *splits);
 
 /* KV compaction ("Ground Truth in Silicon ...", section "Why This Message Was
  * Written": KV-cache defragmentation).  For every sequence b and logical

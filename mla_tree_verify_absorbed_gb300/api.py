@@ -28,7 +28,8 @@ DEVERR = {
 
 # every symbol include/*.h declares
 EXPORTS = ("mla_verify_workspace_size", "mla_verify_attn", "mla_verify_attn_noalloc", "mla_verify_noalloc_check",
-           "mla_verify_build_meta", "mla_verify_check", "mla_status_str", "mla_verify_abi_version",
+           "mla_verify_build_meta", "mla_verify_check", "mla_verify_splits_used", "mla_status_str",
+           "mla_verify_abi_version",
            "mla_verify_selftest_timeout", "mla_kv_compact", "mla_ddtree_build", "mla_ddtree_accept")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 DDTREE_WORKSPACE_BYTES = 256
@@ -99,6 +100,8 @@ def load(path: Optional[str] = None):
     lib.mla_verify_attn_noalloc.argtypes = [ctypes.POINTER(MlaVerifyArgs), ctypes.c_int, ctypes.c_void_p]
     lib.mla_verify_noalloc_check.restype = ctypes.c_int
     lib.mla_verify_noalloc_check.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
+    lib.mla_verify_splits_used.restype = ctypes.c_int
+    lib.mla_verify_splits_used.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
     lib.mla_verify_build_meta.restype = ctypes.c_int
     lib.mla_verify_build_meta.argtypes = [ctypes.POINTER(MlaVerifyArgs), ctypes.c_void_p, ctypes.c_size_t,
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
@@ -408,6 +411,17 @@ def check(workspace, stream=None) -> int:
     if st not in (MLA_OK, MLA_ERR_DEVICE_CHECK):
         raise MlaError(st, "mla_verify_check")
     return int(bits.value)
+
+
+def splits_used(workspace, stream=None) -> int:
+    """Synchronise and return the split count the last verify_attn call on
+    this workspace used (the library's choice when num_splits was 0)."""
+    v = ctypes.c_int32(0)
+    st = load().mla_verify_splits_used(ctypes.c_void_p(_ptr(workspace)), _stream(stream), ctypes.byref(v))
+    if st != MLA_OK:
+        raise MlaError(st, "mla_verify_splits_used")
+    return int(v.value)
+
 
 
 # ----------------------------------------------------------------------------

@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(kSimtThreads, 2) attn_simt_kernel(Params p) {
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int64_t item = blockIdx.x; item < p.n_items; item += gridDim.x) {
-    const Item sg = item_at(p, item);
+    const Item sg = item_at(p, p.splits, item);
     if (sg.t1 <= sg.t0) continue;  // empty chunk (sequence shorter than the split count)
     const int b = sg.b;
     const int64_t P = p.prefix_lens[b];

@@ -33,8 +33,9 @@ namespace {
 struct Plan {
   int algo;        // MLA_ALGO_SIMT or MLA_ALGO_TC (resolved)
   int rg, tk, groups;
-  int splits;      // KV chunks per row group
+  int splits;      // KV chunks per row group (S_max when auto_plan)
   int64_t items;   // B * splits * groups
+  bool auto_plan;  // the metadata kernel picks the split count in [1, splits]
   int grid;        // CTAs (SIMT) or clusters (TC), persistent over items
   int sm_count;
   WsLayout L;
@@ -146,6 +147,9 @@ mla_status make_plan(const mla_verify_args* a, int num_splits, Plan* pl) {
     slots = (algo == MLA_ALGO_TC) ? tc_clusters_per_gpu(pl->sm_count) : simt_ctas_per_gpu(pl->sm_count);
     if (slots < 1) slots = 1;
     pl->splits = auto_splits(row_groups, slots);
+    // the tensor-core kernel's split count is then fixed on the device, from
+    // the sequences' lengths, within [1, splits]
+    pl->auto_plan = (algo == MLA_ALGO_TC);
   } else {
     pl->splits = num_splits;
   }
@@ -187,8 +191,10 @@ Params make_params(const mla_verify_args* a, const Plan& pl, void* ws) {
   p.splits = pl.splits;
   p.n_items = pl.items;
   p.grid = pl.grid;
+  p.auto_plan = pl.auto_plan ? 1 : 0;
   char* base = static_cast<char*>(ws);
   p.err = reinterpret_cast<uint32_t*>(base + pl.L.err);
+  p.plan = reinterpret_cast<int32_t*>(base + pl.L.plan);
   p.anc = reinterpret_cast<uint64_t*>(base + pl.L.anc);
   p.seq_tiles = reinterpret_cast<int32_t*>(base + pl.L.seq_tiles);
   p.seq_kv_base = reinterpret_cast<int64_t*>(base + pl.L.seq_kv_base);
@@ -339,6 +345,18 @@ mla_status mla_verify_check(const void* workspace, mla_stream_t stream, uint32_t
   if (cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
   if (bits) *bits = v;
   return v ? MLA_ERR_DEVICE_CHECK : MLA_OK;
+}
+
+mla_status mla_verify_splits_used(const void* workspace, mla_stream_t stream, int32_t* splits) {
+  if (!workspace) return MLA_ERR_WORKSPACE;
+  if (!splits) return MLA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+  // the split count sits at offset 256 of every workspace layout
+  int32_t v = 0;
+  if (cudaMemcpy(&v, static_cast<const char*>(workspace) + 256, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  *splits = v;
+  return MLA_OK;
 }
 
 const char* mla_status_str(mla_status s) {

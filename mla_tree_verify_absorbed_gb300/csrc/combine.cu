@@ -4,97 +4,102 @@
 // partial output o_s and log-sum-exp lse_s per non-empty chunk.  Exactly:
 //   lse = ln sum_s exp(lse_s),   out = sum_s exp(lse_s - lse) * o_s,
 // because each piece's softmax over its own tokens, reweighted by its share
-// of the total exponent mass, is the softmax over the union.  With one chunk
-// per row group the attention kernel wrote the results directly and this
-// kernel is not launched.
+// of the total exponent mass, is the softmax over the union.  When a call
+// keeps one chunk per row group the attention kernel writes the results
+// directly: this kernel is then not launched, or (the split count being chosen
+// on the device) returns at once.
 #include "common.cuh"
 
 namespace mlav {
 
-constexpr int kCombineThreads = 256;  // 8 warps; one warp per (row, quarter of the 512 columns)
-constexpr int kQuarters = 4;          // 128 columns per warp: one float4 per lane
+constexpr int kCombineThreads = 256;  // 8 warps; one warp per output row
+constexpr int kPieceBatch = 4;        // pieces whose partial rows are loaded together
 
+// Lane l of a row's warp holds columns 4 (l + 32 q) .. + 3, q = 0..3, of the
+// row: every access of the warp covers 512 contiguous bytes.
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params p) {
   grid_dep_wait();  // the attention kernel's partials and error word
-  if (*p.err) return;
+  // nothing to merge when the attention kernel wrote the outputs itself (S = 1)
+  if (*p.err || *p.plan == 1) return;
   const int lane = threadIdx.x & 31;
-  const int64_t gw = (int64_t)blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5);
-  const int64_t total_rows = (int64_t)p.B * p.rows;
-  if (gw >= total_rows * kQuarters) return;
-  const int64_t grow = gw / kQuarters;
-  const int quarter = (int)(gw % kQuarters);
+  const int64_t grow = (int64_t)blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5);
+  if (grow >= (int64_t)p.B * p.rows) return;
   const int b = (int)(grow / p.rows);
   const int row = (int)(grow % p.rows);
   const int g = row / p.rg;
-  const int64_t T = p.seq_tiles[b];
-  const int S = p.splits;
   const int r = row - g * p.rg;
-  auto item_of = [&](int k) { return ((int64_t)b * S + k) * p.groups + g; };
-  auto nonempty = [&](int k) { return ((int64_t)(k + 1) * T) / S > ((int64_t)k * T) / S; };
-  // pass 1: the lanes read the pieces' lse in parallel; warp max
+  const int64_t T = p.seq_tiles[b];
+  int S = *p.plan;  // the split count the attention kernel used
+  if (S < 1 || S > p.splits) S = p.splits;
+  // partial row of piece k (chunk k of row group g of sequence b)
+  auto prow = [&](int k) { return (((int64_t)b * S + k) * p.groups + g) * p.rg + r; };
+  // an empty chunk was skipped by the attention kernel: its slot holds stale bytes
+  auto live = [&](int k) { return k < S && ((int64_t)(k + 1) * T) / S > ((int64_t)k * T) / S; };
+  float4 v[kPieceBatch][4];
+  auto load_batch = [&](int k0) {
+#pragma unroll
+    for (int u = 0; u < kPieceBatch; ++u) {
+      if (live(k0 + u)) {
+        const float4* src = reinterpret_cast<const float4*>(p.part_o + prow(k0 + u) * kDl);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[u][q] = src[lane + 32 * q];
+      }
+    }
+  };
+  // the first pieces' rows are in flight while the largest lse is found
+  load_batch(0);
   float M = -INFINITY;
   for (int k = lane; k < S; k += 32)
-    if (nonempty(k)) M = fmaxf(M, p.part_lse[item_of(k) * p.rg + r]);
+    if (live(k)) M = fmaxf(M, p.part_lse[prow(k)]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  // pass 2: weights exp(lse_k - M) (lane k % 32 holds piece k's), warp sum, and
-  // the weighted sum of the pieces' outputs in piece order.  The loads of
-  // kBatch pieces are issued before any is used; a piece with weight 0 (empty,
-  // or beyond S) loads from piece k0, which is always allocated, and its value
-  // is never used, so nothing it holds reaches the sum.
-  constexpr int kBatch = 8;
+  // weights exp(lse_k - M) <= 1, summed in piece order; pieces with weight 0
+  // (empty, or an lse of -inf) add nothing
   float L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 acc[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != -INFINITY) {
-    for (int k0 = 0; k0 < S; k0 += 32) {
-      const int k = k0 + lane;
-      const float wk = (k < S && nonempty(k)) ? __expf(p.part_lse[item_of(k) * p.rg + r] - M) : 0.f;
-      float wsum = wk;
+    for (int k0 = 0; k0 < S; k0 += kPieceBatch) {
+      if (k0 > 0) load_batch(k0);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-      L += wsum;
-      const int n = S - k0 < 32 ? S - k0 : 32;
-      for (int q0 = 0; q0 < n; q0 += kBatch) {
-        float w[kBatch];
-        float4 v[kBatch];
+      for (int u = 0; u < kPieceBatch; ++u) {
+        if (!live(k0 + u)) continue;
+        const float w = __expf(p.part_lse[prow(k0 + u)] - M);
+        if (w == 0.f) continue;
+        L += w;
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          w[u] = __shfl_sync(0xffffffffu, wk, (q0 + u) & 31);
-          if (q0 + u >= n) w[u] = 0.f;
-          const int kk = w[u] != 0.f ? k0 + q0 + u : k0;
-          v[u] = reinterpret_cast<const float4*>(p.part_o + (item_of(kk) * p.rg + r) * kDl)[quarter * 32 + lane];
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          if (w[u] != 0.f) {
-            acc.x = fmaf(w[u], v[u].x, acc.x);
-            acc.y = fmaf(w[u], v[u].y, acc.y);
-            acc.z = fmaf(w[u], v[u].z, acc.z);
-            acc.w = fmaf(w[u], v[u].w, acc.w);
-          }
+        for (int q = 0; q < 4; ++q) {
+          acc[q].x = fmaf(w, v[u][q].x, acc[q].x);
+          acc[q].y = fmaf(w, v[u][q].y, acc[q].y);
+          acc[q].z = fmaf(w, v[u][q].z, acc[q].z);
+          acc[q].w = fmaf(w, v[u][q].w, acc[q].w);
         }
       }
     }
   }
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
   const int64_t orow = (int64_t)b * p.rows + row;
-  const int64_t d = (int64_t)4 * (quarter * 32 + lane);
-  if (p.dtype == MLA_BF16) {
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-    uint2 w2;
-    w2.x = *reinterpret_cast<uint32_t*>(&lo);
-    w2.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDl + d) = w2;
-  } else {
-    *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow * kDl + d) =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int64_t d = (int64_t)4 * (lane + 32 * q);
+    if (p.dtype == MLA_BF16) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc[q].x * inv, acc[q].y * inv);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc[q].z * inv, acc[q].w * inv);
+      uint2 w2;
+      w2.x = *reinterpret_cast<uint32_t*>(&lo);
+      w2.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDl + d) = w2;
+    } else {
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow * kDl + d) =
+          make_float4(acc[q].x * inv, acc[q].y * inv, acc[q].z * inv, acc[q].w * inv);
+    }
   }
-  if (quarter == 0 && lane == 0 && p.lse) p.lse[orow] = (L > 0.f) ? M + logf(L) : -INFINITY;
+  if (lane == 0 && p.lse) p.lse[orow] = (L > 0.f) ? M + logf(L) : -INFINITY;
 }
 
 cudaError_t launch_combine(const Params& p, cudaStream_t stream, bool pdl) {
-  const int64_t warps = (int64_t)p.B * p.rows * kQuarters;
+  const int64_t warps = (int64_t)p.B * p.rows;
   const int64_t blocks = (warps + (kCombineThreads / 32) - 1) / (kCombineThreads / 32);
   if (blocks == 0) return cudaSuccess;
   return launch_kernel(combine_kernel, dim3((unsigned)blocks), dim3(kCombineThreads), 0, stream, pdl, p);

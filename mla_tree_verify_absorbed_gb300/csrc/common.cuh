@@ -39,19 +39,22 @@ struct Params {
   void* out;
   float* lse;
 
-  // partition: work item i = (b * splits + k) * groups + g covers row group g
-  // of sequence b over KV chunk k (tiles [k*T_b/splits, (k+1)*T_b/splits)).
-  // Chunk-major order puts the row groups of one chunk next to each other, so
-  // items running at the same time read the same KV from L2.
+  // partition: work item i = (b * S + k) * groups + g covers row group g of
+  // sequence b over KV chunk k (tiles [k*T_b/S, (k+1)*T_b/S)), S the split
+  // count of the call (*plan).  Chunk-major order puts the row groups of one
+  // chunk next to each other, so items running at the same time read the same
+  // KV from L2.
   int rg;            // rows per row group
   int groups;        // G = ceil(rows / rg)
   int tk;            // tokens per tile
-  int splits;        // S: KV chunks per row group
-  int64_t n_items;   // B * S * G
+  int splits;        // S_max: the workspace holds partials for B * S_max * G items
+  int64_t n_items;   // B * S_max * G
   int grid;          // CTAs (or clusters) taking items round-robin
+  int auto_plan;     // 1: the metadata kernel picks S in [1, S_max]; 0: S = S_max
 
   // workspace views
   uint32_t* err;
+  int32_t* plan;           // [2] S and the grid it assumed, written by the metadata kernel
   uint64_t* anc;           // [B][Q]
   int32_t* seq_tiles;      // [B]   T_b = ceil(N_b / tk)
   int64_t* seq_kv_base;    // [B+1] cumulative N_b
@@ -64,10 +67,11 @@ struct Params {
 };
 
 // ---------------------------------------------------------------------------
-// Workspace layout: fixed regions, each 256-byte aligned.
+// Workspace layout: fixed regions, each 256-byte aligned; the error words sit
+// at offset 0 and the split count at offset 256 of every layout.
 // ---------------------------------------------------------------------------
 struct WsLayout {
-  size_t err, anc, seq_tiles, seq_kv_base, part_lse, part_o, total;
+  size_t err, plan, anc, seq_tiles, seq_kv_base, part_lse, part_o, total;
   int64_t part_slots;
 };
 
@@ -77,6 +81,7 @@ inline WsLayout ws_layout(int B, int Q, int rg, int64_t part_slots) {
   WsLayout L;
   size_t o = 0;
   L.err = o;          o = align256(o + 16);
+  L.plan = o;         o = align256(o + 16);
   L.anc = o;          o = align256(o + sizeof(uint64_t) * (size_t)B * (size_t)Q + 8);
   L.seq_tiles = o;    o = align256(o + sizeof(int32_t) * (size_t)B + 4);
   L.seq_kv_base = o;  o = align256(o + sizeof(int64_t) * ((size_t)B + 1));
@@ -142,15 +147,16 @@ struct Item {
   int t0, t1;
 };
 
-__device__ __forceinline__ Item item_at(const Params& p, int64_t i) {
+// Item i of a call that cuts each row group's KV into S chunks.
+__device__ __forceinline__ Item item_at(const Params& p, int S, int64_t i) {
   Item it;
   it.g = (int)(i % p.groups);
   const int64_t bk = i / p.groups;
-  it.k = (int)(bk % p.splits);
-  it.b = (int)(bk / p.splits);
+  it.k = (int)(bk % S);
+  it.b = (int)(bk / S);
   const int64_t T = p.seq_tiles[it.b];
-  it.t0 = (int)((it.k * T) / p.splits);
-  it.t1 = (int)(((it.k + 1) * T) / p.splits);
+  it.t0 = (int)((it.k * T) / S);
+  it.t1 = (int)(((it.k + 1) * T) / S);
   return it;
 }
 

@@ -32,13 +32,69 @@ __device__ int64_t block_inclusive_scan(int64_t v, int64_t* sh) {
   return r;
 }
 
+// Split plan of the tensor-core kernel when the caller leaves the split count
+// to the library.  The host sizes the workspace for S_max = p.splits chunks per
+// row group (the count that fills the clusters in whole waves, from B, H and Q
+// alone); once the tile counts T_b are known, every S in [1, S_max] is scored
+// by the time it would take and the cheapest is used (the smaller on a tie).
+// The persistent clusters take items round-robin (item i runs on cluster
+// i mod grid), so the attention time is the most loaded cluster's sum over its
+// non-empty items of (fixed cost + tiles); S > 1 adds the combine kernel's pass
+// over the fp32 partials.  The constants are GB300 measurements of this
+// library's kernels: ~1 us per 64-token tile per cluster, ~14 tiles' worth of
+// fixed cost per item (query staging, pipeline fill and drain, the epilogue),
+// and a combine moving ~3 TB/s plus ~3 us of launch and tail.  Integer
+// arithmetic throughout, so the same lengths always give the same S.  One warp
+// scores one candidate at a time; lanes add item costs into the warp's
+// per-cluster totals in shared memory.
+constexpr int kPlanMaxClusters = 64;
+constexpr int kPlanMaxSplits = 64;
+constexpr unsigned long long kPlanItemTiles = 14;
+constexpr int64_t kPlanTileNs = 1000;
+constexpr int64_t kPlanCombineBytesPerNs = 3000;
+constexpr int64_t kPlanCombineFixedNs = 3000;
+
+__device__ void plan_scores(const Params& p, unsigned long long* load, int64_t* cost) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int C = p.grid;
+  unsigned long long* ld = load + warp * kPlanMaxClusters;
+  for (int S = warp + 1; S <= p.splits; S += kMetaThreads / 32) {
+    for (int c = lane; c < C; c += 32) ld[c] = 0ull;
+    __syncwarp();
+    const int64_t n = (int64_t)p.B * p.groups * S;
+    for (int64_t i = lane; i < n; i += 32) {
+      const int64_t bk = i / p.groups;
+      const int64_t k = bk % S;
+      const int64_t T = p.seq_tiles[bk / S];
+      const int64_t t = ((k + 1) * T) / S - (k * T) / S;
+      if (t > 0) atomicAdd(&ld[i % C], kPlanItemTiles + (unsigned long long)t);
+    }
+    __syncwarp();
+    unsigned long long mx = 0ull;
+    for (int c = lane; c < C; c += 32) mx = ld[c] > mx ? ld[c] : mx;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long v = __shfl_xor_sync(0xffffffffu, mx, o);
+      mx = v > mx ? v : mx;
+    }
+    if (lane == 0) {
+      int64_t ns = (int64_t)mx * kPlanTileNs;
+      if (S > 1) ns += (int64_t)p.B * p.rows * S * (kDl * 4) / kPlanCombineBytesPerNs + kPlanCombineFixedNs;
+      cost[S - 1] = ns;
+    }
+    __syncwarp();
+  }
+}
+
 // One block.  Clears the error word, validates prefix_lens / kv_indptr /
 // page capacity, computes T_b = ceil(N_b / tk) and the prefix sums
-// seq_kv_base of N_b (a thread per sequence), then validates the parents and
-// builds anc (a thread per node).
+// seq_kv_base of N_b (a thread per sequence), fixes the call's split count,
+// then validates the parents and builds anc (a thread per node).
 __global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
   __shared__ int64_t sh[kMetaThreads];
   __shared__ int64_t carry_kv;
+  __shared__ unsigned long long plan_load[(kMetaThreads / 32) * kPlanMaxClusters];
+  __shared__ int64_t plan_cost[kPlanMaxSplits];
   const int tid = threadIdx.x;
   grid_dep_launch();  // the slot pass may start launching; it waits for this kernel
   if (tid == 0) {
@@ -79,6 +135,23 @@ __global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
       carry_kv += k_inc;
     }
     __syncthreads();
+  }
+
+  // the split count of this call (the tile counts above are visible to the
+  // whole block after the loop's last barrier)
+  if (p.auto_plan && p.splits > 1 && p.splits <= kPlanMaxSplits && p.grid >= 1 && p.grid <= kPlanMaxClusters) {
+    plan_scores(p, plan_load, plan_cost);
+    __syncthreads();
+    if (tid == 0) {
+      int best = 1;
+      for (int S = 2; S <= p.splits; ++S)
+        if (plan_cost[S - 1] < plan_cost[best - 1]) best = S;
+      p.plan[0] = best;
+      p.plan[1] = p.grid;  // the cluster count the choice assumed (diagnostics)
+    }
+  } else if (tid == 0) {
+    p.plan[0] = p.splits;
+    p.plan[1] = p.grid;
   }
 
   // ancestor-or-self masks
