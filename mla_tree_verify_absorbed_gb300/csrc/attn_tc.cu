@@ -192,15 +192,25 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Calls f(item, it) for the non-empty items of this cluster, in order, for a
-// call with S KV chunks per row group.
+// Calls f(slot, it) for the non-empty work units of this cluster (see Split),
+// in order.  slot is the unit's partial-output slot, or -1 when the unit is a
+// row group's only piece and writes the outputs itself.
 template <class F>
-__device__ __forceinline__ void for_items(const Params& p, int S, int cluster_id, int n_clusters, F&& f) {
-  const int64_t n_items = (int64_t)p.B * p.groups * S;
-  for (int64_t item = cluster_id; item < n_items; item += n_clusters) {
-    const Item it = item_at(p, S, item);
+__device__ __forceinline__ void for_items(const Params& p, const Split& sc, int cluster_id, int n_clusters, F&& f) {
+  const int64_t n_units = sc.tail + (sc.n_items - sc.tail) * sc.P;
+  for (int64_t u = cluster_id; u < n_units; u += n_clusters) {
+    const bool piece = u >= sc.tail && sc.P > 1;
+    const int64_t v = u - sc.tail;
+    const int64_t item = piece ? sc.tail + v / sc.P : u;
+    const int64_t slot = piece ? v : (sc.S > 1 ? u : -1);
+    Item it = item_at(p, sc.S, item);
+    if (piece) {
+      const int64_t q = v % sc.P, a = it.t0, len = it.t1 - it.t0;
+      it.t0 = (int)(a + q * len / sc.P);
+      it.t1 = (int)(a + (q + 1) * len / sc.P);
+    }
     if (it.t1 <= it.t0) continue;
-    if (!f(item, it)) return;
+    if (!f(slot, it)) return;
   }
 }
 
@@ -218,7 +228,7 @@ __device__ __forceinline__ void for_items(const Params& p, int S, int cluster_id
 //     for nh = 0, 1; warp pw copies 8 tokens, one instruction per token (lane
 //     l moves piece l & 15 of segment nh = l >> 4).
 // Positions past the sequence read slot 0; the softmax gives them zero weight.
-__device__ void producer(const Params& p, int S, uint8_t* smem, Ctl* c, int pw, uint32_t rank, int cluster_id,
+__device__ void producer(const Params& p, const Split sc, uint8_t* smem, Ctl* c, int pw, uint32_t rank, int cluster_id,
                          int n_clusters) {
   const int lane = threadIdx.x & 31;
   const bool score = rank < 2;
@@ -231,7 +241,7 @@ __device__ void producer(const Params& p, int S, uint8_t* smem, Ctl* c, int pw, 
   const __nv_bfloat16* kpe_g = reinterpret_cast<const __nv_bfloat16*>(p.k_pe);
   const uint32_t sbase = smem_u32(smem);
   int j = 0;
-  for_items(p, S, cluster_id, n_clusters, [&](int64_t, const Item& it) {
+  for_items(p, sc, cluster_id, n_clusters, [&](int64_t, const Item& it) {
     const int b = it.b;
     const int64_t N = (int64_t)p.prefix_lens[b] + p.Q;
     const int64_t idx0 = p.page_size == 1 ? (int64_t)p.kv_indptr[b] : 0;
@@ -296,10 +306,10 @@ __device__ void producer(const Params& p, int S, uint8_t* smem, Ctl* c, int pw, 
 
 // Odd CTAs: tell the pair's MMA-issuing CTA when this CTA's share of a tile
 // has landed (whole warp).
-__device__ void relay(const Params& p, int S, Ctl* c, uint32_t leader, int cluster_id, int n_clusters) {
+__device__ void relay(const Params& p, const Split sc, Ctl* c, uint32_t leader, int cluster_id, int n_clusters) {
   const int nst = leader == 0 ? kStagesS : kStagesV;
   int j = 0;
-  for_items(p, S, cluster_id, n_clusters, [&](int64_t, const Item& it) {
+  for_items(p, sc, cluster_id, n_clusters, [&](int64_t, const Item& it) {
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       const int s = j % nst;
       if (!wait_warp(&c->full[s], (uint32_t)(j / nst) & 1u, c, kSiteRelay, j)) return false;
@@ -314,7 +324,7 @@ __device__ void relay(const Params& p, int S, Ctl* c, uint32_t leader, int clust
 // ---------------------------------------------------------------------------
 // score pair
 // ---------------------------------------------------------------------------
-__device__ void score_mma(const Params& p, int S, uint8_t* smem, Ctl* c, int cluster_id, int n_clusters) {
+__device__ void score_mma(const Params& p, const Split sc, uint8_t* smem, Ctl* c, int cluster_id, int n_clusters) {
   // rank 0, whole warp; one elected lane issues each pair MMA.  While the
   // tensor pipe works through a tile's MMAs, the warp checks (without
   // blocking) whether the next tile can start, so the checks cost no pipe time.
@@ -336,7 +346,7 @@ __device__ void score_mma(const Params& p, int S, uint8_t* smem, Ctl* c, int clu
                     (jj < 2 || mbar_test_wait_cluster(&c->s_free[jj & 1], (((uint32_t)jj >> 1) & 1u) ^ 1u));
     return __all_sync(0xffffffffu, ok);
   };
-  for_items(p, S, cluster_id, n_clusters, [&](int64_t, const Item& it) {
+  for_items(p, sc, cluster_id, n_clusters, [&](int64_t, const Item& it) {
     if (!wait_warp(&c->q_ready, (uint32_t)seg & 1u, c, kSiteQReady, j)) return false;
     tc_fence_after();
     bool ready = false;
@@ -378,7 +388,7 @@ __device__ void score_mma(const Params& p, int S, uint8_t* smem, Ctl* c, int clu
 // every tile: they exchange partial maxima per tile through shared memory, so
 // both follow the same running max, and keep partial row sums that are added
 // once per item.
-__device__ void score_softmax(const Params& p, int S, uint8_t* smem, Ctl* c, uint32_t rank, int cluster_id,
+__device__ void score_softmax(const Params& p, const Split sc, uint8_t* smem, Ctl* c, uint32_t rank, int cluster_id,
                               int n_clusters) {
   const int lane = threadIdx.x & 31;
   const int w = (threadIdx.x >> 5) - kWarpRows;     // 0..7
@@ -394,7 +404,7 @@ __device__ void score_softmax(const Params& p, int S, uint8_t* smem, Ctl* c, uin
   const float sl2 = p.scale_log2;
   const int nq = p.Q;
   int j = 0, seg = 0;
-  for_items(p, S, cluster_id, n_clusters, [&](int64_t, const Item& it) {
+  for_items(p, sc, cluster_id, n_clusters, [&](int64_t, const Item& it) {
     const int b = it.b;
     const int row = it.g * kRG + (int)rank * kRC + r;
     const bool live = row < p.rows;
@@ -531,11 +541,11 @@ __device__ void score_softmax(const Params& p, int S, uint8_t* smem, Ctl* c, uin
 
 // Score CTAs, one thread: ships each staged P tile and its rescale factors to
 // the value partner with two bulk copies whose bytes complete its p_full.
-__device__ void p_copier(const Params& p, int S, uint8_t* smem, Ctl* c, uint32_t rank, int cluster_id,
+__device__ void p_copier(const Params& p, const Split sc, uint8_t* smem, Ctl* c, uint32_t rank, int cluster_id,
                          int n_clusters) {
   const uint32_t partner = rank + 2;
   int j = 0;
-  for_items(p, S, cluster_id, n_clusters, [&](int64_t, const Item& it) {
+  for_items(p, sc, cluster_id, n_clusters, [&](int64_t, const Item& it) {
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       const int sb = j & 1;
       if (!wait(&c->p_staged[sb], (uint32_t)(j >> 1) & 1u, c, kSitePStaged, j)) return false;
@@ -553,7 +563,7 @@ __device__ void p_copier(const Params& p, int S, uint8_t* smem, Ctl* c, uint32_t
 // ---------------------------------------------------------------------------
 // value pair
 // ---------------------------------------------------------------------------
-__device__ void value_mma(const Params& p, int S, uint8_t* smem, Ctl* c, int cluster_id, int n_clusters) {
+__device__ void value_mma(const Params& p, const Split sc, uint8_t* smem, Ctl* c, int cluster_id, int n_clusters) {
   // rank 2, whole warp; one elected lane issues each pair MMA, and checks
   // (without blocking) whether the next tile can start while these run
   const uint32_t tO = c->tmem_base;
@@ -565,7 +575,7 @@ __device__ void value_mma(const Params& p, int S, uint8_t* smem, Ctl* c, int clu
                     mbar_test_wait_cluster(&c->o_ready[jj & 1], (uint32_t)(jj >> 1) & 1u);
     return __all_sync(0xffffffffu, ok);
   };
-  for_items(p, S, cluster_id, n_clusters, [&](int64_t, const Item& it) {
+  for_items(p, sc, cluster_id, n_clusters, [&](int64_t, const Item& it) {
     bool ready = false;
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       const int s = j % kStagesV, pb = j & 1;
@@ -603,9 +613,9 @@ __device__ void value_mma(const Params& p, int S, uint8_t* smem, Ctl* c, int clu
 
 // Releases each tile's P buffer back to the score partner once the PV MMAs
 // that read it have completed (one thread).
-__device__ void value_release(const Params& p, int S, Ctl* c, uint32_t rank, int cluster_id, int n_clusters) {
+__device__ void value_release(const Params& p, const Split sc, Ctl* c, uint32_t rank, int cluster_id, int n_clusters) {
   int j = 0;
-  for_items(p, S, cluster_id, n_clusters, [&](int64_t, const Item& it) {
+  for_items(p, sc, cluster_id, n_clusters, [&](int64_t, const Item& it) {
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       if (!wait(&c->pv_done[j & 1], (uint32_t)(j >> 1) & 1u, c, kSiteRelease, j)) return false;
       mbar_arrive_cluster_relaxed(&c->p_free[j & 1], rank - 2);
@@ -618,7 +628,7 @@ __device__ void value_release(const Params& p, int S, Ctl* c, uint32_t rank, int
 // per tile, wait for P, rescale this warp's O rows when a factor differs from
 // 1, and tell the MMA-issuing CTA that O is ready; per item, normalise O and
 // write the outputs (or the split partials).
-__device__ void value_rows(const Params& p, int S, Ctl* c, uint32_t rank, int cluster_id, int n_clusters) {
+__device__ void value_rows(const Params& p, const Split sc, Ctl* c, uint32_t rank, int cluster_id, int n_clusters) {
   const int lane = threadIdx.x & 31;
   const int w = (threadIdx.x >> 5) - kWarpRows;  // 0..7
   const int wq = w & 3;
@@ -629,7 +639,7 @@ __device__ void value_rows(const Params& p, int S, Ctl* c, uint32_t rank, int cl
   const uint32_t tO = c->tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)col0;
   const float ln2 = 0.69314718055994530942f;
   int j = 0, seg = 0;
-  for_items(p, S, cluster_id, n_clusters, [&](int64_t item, const Item& it) {
+  for_items(p, sc, cluster_id, n_clusters, [&](int64_t slot, const Item& it) {
     for (int t = it.t0; t < it.t1; ++t, ++j) {
       const int pb = j & 1;
       if (w == 0 && lane == 0) mbar_arrive_expect_tx(&c->p_full[pb], kPTxBytes);
@@ -670,7 +680,7 @@ __device__ void value_rows(const Params& p, int S, Ctl* c, uint32_t rank, int cl
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const float lse = l > 0.f ? (m + log2f(l)) * ln2 : -INFINITY;
     const int64_t orow = (int64_t)it.b * p.rows + row;
-    if (S == 1) {
+    if (slot < 0) {
       uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDl);
 #pragma unroll 1
       for (int c0 = 0; c0 < 256; c0 += 32) {
@@ -691,7 +701,7 @@ __device__ void value_rows(const Params& p, int S, Ctl* c, uint32_t rank, int cl
       }
       if (live && p.lse && h == 0) p.lse[orow] = lse;
     } else {
-      const int64_t prow = item * kRG + half * kRC + r;
+      const int64_t prow = slot * kRG + half * kRC + r;
       float4* dst = reinterpret_cast<float4*>(p.part_o + prow * kDl);
 #pragma unroll 1
       for (int c0 = 0; c0 < 256; c0 += 32) {
@@ -769,25 +779,22 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads,
 
   const int cluster_id = blockIdx.x / kClusterCtas;
   const int n_clusters = gridDim.x / kClusterCtas;
-  // this call's split count, from the metadata kernel (the clamp only keeps
-  // item indices inside the workspace whatever the word holds)
-  int S = *p.plan;
-  if (S < 1 || S > p.splits) S = p.splits;
+  const Split sc = read_split(p);  // this call's work split, from the metadata kernel
   const bool score = rank < 2;
   if (warp < kProducerWarps) {
-    producer(p, S, smem, c, warp, rank, cluster_id, n_clusters);
+    producer(p, sc, smem, c, warp, rank, cluster_id, n_clusters);
   } else if (warp == kWarpMma) {
-    if (!leader) relay(p, S, c, rank & 2u, cluster_id, n_clusters);
-    else if (score) score_mma(p, S, smem, c, cluster_id, n_clusters);
-    else value_mma(p, S, smem, c, cluster_id, n_clusters);
+    if (!leader) relay(p, sc, c, rank & 2u, cluster_id, n_clusters);
+    else if (score) score_mma(p, sc, smem, c, cluster_id, n_clusters);
+    else value_mma(p, sc, smem, c, cluster_id, n_clusters);
   } else if (warp == kWarpAux) {
     if ((threadIdx.x & 31) == 0) {
-      if (score) p_copier(p, S, smem, c, rank, cluster_id, n_clusters);
-      else value_release(p, S, c, rank, cluster_id, n_clusters);
+      if (score) p_copier(p, sc, smem, c, rank, cluster_id, n_clusters);
+      else value_release(p, sc, c, rank, cluster_id, n_clusters);
     }
   } else if (warp >= kWarpRows && warp < kWarpRows + kRowWarps) {
-    if (score) score_softmax(p, S, smem, c, rank, cluster_id, n_clusters);
-    else value_rows(p, S, c, rank, cluster_id, n_clusters);
+    if (score) score_softmax(p, sc, smem, c, rank, cluster_id, n_clusters);
+    else value_rows(p, sc, c, rank, cluster_id, n_clusters);
   }
 
   __syncwarp();

@@ -155,7 +155,11 @@ mla_status make_plan(const mla_verify_args* a, int num_splits, Plan* pl) {
   }
   pl->items = row_groups * pl->splits;
   if (pl->items > ((int64_t)1 << 26)) return MLA_ERR_UNSUPPORTED;
-  pl->L = ws_layout(a->B, a->Q, pl->rg, pl->splits > 1 ? pl->items : 0);
+  int64_t part_slots = pl->splits > 1 ? pl->items : 0;
+  // an automatic plan may keep one chunk per row group and cut the items of a
+  // partial last wave into pieces, at most one per cluster
+  if (pl->auto_plan && part_slots < slots) part_slots = slots;
+  pl->L = ws_layout(a->B, a->Q, pl->rg, part_slots);
   return MLA_OK;
 }
 
@@ -200,6 +204,7 @@ Params make_params(const mla_verify_args* a, const Plan& pl, void* ws) {
   p.seq_kv_base = reinterpret_cast<int64_t*>(base + pl.L.seq_kv_base);
   p.part_lse = reinterpret_cast<float*>(base + pl.L.part_lse);
   p.part_o = reinterpret_cast<float*>(base + pl.L.part_o);
+  p.part_slots = pl.L.part_slots;
   return p;
 }
 
@@ -263,7 +268,8 @@ mla_status run_attn(const mla_verify_args* a, void* workspace, size_t ws_bytes, 
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   if (a->profile_events && cudaEventRecord((cudaEvent_t)a->profile_events[1], s) != cudaSuccess)
     return MLA_ERR_CUDA;
-  if (pl.splits > 1 && launch_combine(p, s, pdl) != cudaSuccess) return MLA_ERR_CUDA;
+  // the combine returns at once when the device plan kept every row group whole
+  if ((pl.splits > 1 || pl.auto_plan) && launch_combine(p, s, pdl) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }
 }  // namespace

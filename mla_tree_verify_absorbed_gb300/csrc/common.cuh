@@ -54,12 +54,14 @@ struct Params {
 
   // workspace views
   uint32_t* err;
-  int32_t* plan;           // [2] S and the grid it assumed, written by the metadata kernel
+  int32_t* plan;           // [4] written by the metadata kernel: S, the grid it assumed, the first
+                           // item of a tail cut into pieces, pieces per tail item (1: none)
   uint64_t* anc;           // [B][Q]
   int32_t* seq_tiles;      // [B]   T_b = ceil(N_b / tk)
   int64_t* seq_kv_base;    // [B+1] cumulative N_b
-  float* part_lse;         // [n_items][rg]  (natural log)
-  float* part_o;           // [n_items][rg][512], normalised partial outputs
+  float* part_lse;         // [part_slots][rg]  (natural log)
+  float* part_o;           // [part_slots][rg][512], normalised partial outputs
+  int64_t part_slots;      // partial slots the workspace holds (items, or pieces of a split tail)
 
   // failure-detection self-test only (0 otherwise): the tensor-core kernel
   // first waits, at most this many ns, on a barrier nothing completes
@@ -158,6 +160,34 @@ __device__ __forceinline__ Item item_at(const Params& p, int S, int64_t i) {
   it.t0 = (int)((it.k * T) / S);
   it.t1 = (int)(((it.k + 1) * T) / S);
   return it;
+}
+
+// The work split of a call, as the metadata kernel fixed it: S KV chunks per
+// row group give B * G * S items; with P > 1 (only when S = 1), each item from
+// index `tail` on -- the last, partial wave of the persistent grid -- runs as
+// P pieces of its tile range, so that wave keeps every cluster busy.  Work
+// unit u < tail is item u; unit tail + v is piece v % P of item tail + v / P
+// and writes partial slot v.  Words out of range fall back to S_max without
+// pieces: the metadata kernel always writes them, and the checks only keep
+// every index inside the workspace.
+struct Split {
+  int S, P;
+  int64_t tail, n_items;
+};
+
+__device__ __forceinline__ Split read_split(const Params& p) {
+  Split sp;
+  sp.S = p.plan[0];
+  if (sp.S < 1 || sp.S > p.splits) sp.S = p.splits;
+  sp.n_items = (int64_t)p.B * p.groups * sp.S;
+  sp.tail = p.plan[2];
+  sp.P = p.plan[3];
+  if (sp.S != 1 || sp.P < 2 || sp.P > p.grid || sp.tail < 0 || sp.tail > sp.n_items ||
+      (sp.n_items - sp.tail) * sp.P > p.part_slots) {
+    sp.P = 1;
+    sp.tail = sp.n_items;
+  }
+  return sp;
 }
 
 // Sequence owning flat position k of the per-sequence prefix sums `base`.

@@ -35,29 +35,49 @@ __device__ int64_t block_inclusive_scan(int64_t v, int64_t* sh) {
 // Split plan of the tensor-core kernel when the caller leaves the split count
 // to the library.  The host sizes the workspace for S_max = p.splits chunks per
 // row group (the count that fills the clusters in whole waves, from B, H and Q
-// alone); once the tile counts T_b are known, every S in [1, S_max] is scored
-// by the time it would take and the cheapest is used (the smaller on a tie).
-// The persistent clusters take items round-robin (item i runs on cluster
-// i mod grid), so the attention time is the most loaded cluster's sum over its
-// non-empty items of (fixed cost + tiles); S > 1 adds the combine kernel's pass
-// over the fp32 partials.  The constants are GB300 measurements of this
-// library's kernels: ~1 us per 64-token tile per cluster, ~14 tiles' worth of
-// fixed cost per item (query staging, pipeline fill and drain, the epilogue),
-// and a combine moving ~3 TB/s plus ~3 us of launch and tail.  Integer
-// arithmetic throughout, so the same lengths always give the same S.  One warp
-// scores one candidate at a time; lanes add item costs into the warp's
-// per-cluster totals in shared memory.
+// alone) and for at least one partial slot per cluster; once the tile counts
+// T_b are known, every S in [1, S_max] is scored by the time it would take and
+// the cheapest is used (the smaller S on a tie).  The persistent clusters take
+// work units round-robin (unit u runs on cluster u mod grid), so the attention
+// time is the most loaded cluster's sum over its non-empty units of (fixed
+// cost + tiles); S > 1 adds the combine kernel's pass over the fp32 partials.
+// For S = 1 a second form is scored too: when the items fill W >= 1 whole
+// waves and r more items remain, each of those r items runs as
+// P = grid / r >= 2 pieces of its tile range (one unit per idle cluster), and
+// the combine merges just those rows.  The constants are GB300 measurements of
+// this library's kernels: ~1 us per 64-token tile per cluster, ~14 tiles'
+// worth of fixed cost per unit (query staging, pipeline fill and drain, the
+// epilogue), and a combine moving ~3 TB/s plus ~3 us of launch and tail.
+// Integer arithmetic throughout, so the same lengths always give the same
+// plan.  One warp scores one candidate at a time; its lanes add unit costs
+// into the warp's per-cluster totals in shared memory.
 constexpr int kPlanMaxClusters = 64;
 constexpr int kPlanMaxSplits = 64;
-constexpr unsigned long long kPlanItemTiles = 14;
+constexpr unsigned long long kPlanUnitTiles = 14;
 constexpr int64_t kPlanTileNs = 1000;
 constexpr int64_t kPlanCombineBytesPerNs = 3000;
 constexpr int64_t kPlanCombineFixedNs = 3000;
 
-__device__ void plan_scores(const Params& p, unsigned long long* load, int64_t* cost) {
+// The warp's largest per-cluster total, in ns.
+__device__ __forceinline__ int64_t plan_makespan_ns(const unsigned long long* ld, int C) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  unsigned long long mx = 0ull;
+  for (int c = lane; c < C; c += 32) mx = ld[c] > mx ? ld[c] : mx;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long v = __shfl_xor_sync(0xffffffffu, mx, o);
+    mx = v > mx ? v : mx;
+  }
+  return (int64_t)mx * kPlanTileNs;
+}
+
+// cost[S - 1] and pieces[S - 1] (1: no split tail) for S in [1, S_max].
+__device__ void plan_scores(const Params& p, unsigned long long* load, int64_t* cost, int* pieces) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int C = p.grid;
   unsigned long long* ld = load + warp * kPlanMaxClusters;
+  const int64_t rows_bytes = (int64_t)p.rows * (kDl * 4);  // fp32 partial bytes of one sequence's rows
   for (int S = warp + 1; S <= p.splits; S += kMetaThreads / 32) {
     for (int c = lane; c < C; c += 32) ld[c] = 0ull;
     __syncwarp();
@@ -67,20 +87,38 @@ __device__ void plan_scores(const Params& p, unsigned long long* load, int64_t* 
       const int64_t k = bk % S;
       const int64_t T = p.seq_tiles[bk / S];
       const int64_t t = ((k + 1) * T) / S - (k * T) / S;
-      if (t > 0) atomicAdd(&ld[i % C], kPlanItemTiles + (unsigned long long)t);
+      if (t > 0) atomicAdd(&ld[i % C], kPlanUnitTiles + (unsigned long long)t);
     }
-    __syncwarp();
-    unsigned long long mx = 0ull;
-    for (int c = lane; c < C; c += 32) mx = ld[c] > mx ? ld[c] : mx;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long v = __shfl_xor_sync(0xffffffffu, mx, o);
-      mx = v > mx ? v : mx;
+    int64_t best = plan_makespan_ns(ld, C);
+    if (S > 1) best += (int64_t)p.B * S * rows_bytes / kPlanCombineBytesPerNs + kPlanCombineFixedNs;
+    int best_p = 1;
+    const int64_t full = (n / C) * C, r = n - full;
+    if (S == 1 && full > 0 && r > 0 && C / r >= 2) {
+      // the same items, the last r cut into P pieces each
+      const int P = (int)(C / r);
+      __syncwarp();
+      for (int c = lane; c < C; c += 32) ld[c] = 0ull;
+      __syncwarp();
+      for (int64_t i = lane; i < full; i += 32) {
+        const int64_t T = p.seq_tiles[i / p.groups];
+        if (T > 0) atomicAdd(&ld[i % C], kPlanUnitTiles + (unsigned long long)T);
+      }
+      for (int64_t v = lane; v < r * P; v += 32) {
+        const int64_t T = p.seq_tiles[(full + v / P) / p.groups];
+        const int64_t q = v % P;
+        const int64_t t = ((q + 1) * T) / P - (q * T) / P;
+        if (t > 0) atomicAdd(&ld[v], kPlanUnitTiles + (unsigned long long)t);
+      }
+      const int64_t ns = plan_makespan_ns(ld, C) +
+                         r * P * (int64_t)p.rg * (kDl * 4) / kPlanCombineBytesPerNs + kPlanCombineFixedNs;
+      if (ns < best) {
+        best = ns;
+        best_p = P;
+      }
     }
     if (lane == 0) {
-      int64_t ns = (int64_t)mx * kPlanTileNs;
-      if (S > 1) ns += (int64_t)p.B * p.rows * S * (kDl * 4) / kPlanCombineBytesPerNs + kPlanCombineFixedNs;
-      cost[S - 1] = ns;
+      cost[S - 1] = best;
+      pieces[S - 1] = best_p;
     }
     __syncwarp();
   }
@@ -95,6 +133,7 @@ __global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
   __shared__ int64_t carry_kv;
   __shared__ unsigned long long plan_load[(kMetaThreads / 32) * kPlanMaxClusters];
   __shared__ int64_t plan_cost[kPlanMaxSplits];
+  __shared__ int plan_pieces[kPlanMaxSplits];
   const int tid = threadIdx.x;
   grid_dep_launch();  // the slot pass may start launching; it waits for this kernel
   if (tid == 0) {
@@ -137,21 +176,29 @@ __global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
     __syncthreads();
   }
 
-  // the split count of this call (the tile counts above are visible to the
-  // whole block after the loop's last barrier)
-  if (p.auto_plan && p.splits > 1 && p.splits <= kPlanMaxSplits && p.grid >= 1 && p.grid <= kPlanMaxClusters) {
-    plan_scores(p, plan_load, plan_cost);
+  // the work split of this call (the tile counts above are visible to the
+  // whole block after the loop's last barrier): S, the grid assumed, the first
+  // item of a tail cut into pieces, pieces per tail item
+  if (p.auto_plan && p.splits >= 1 && p.splits <= kPlanMaxSplits && p.grid >= 1 &&
+      p.grid <= kPlanMaxClusters && p.part_slots >= p.grid) {
+    plan_scores(p, plan_load, plan_cost, plan_pieces);
     __syncthreads();
     if (tid == 0) {
       int best = 1;
       for (int S = 2; S <= p.splits; ++S)
         if (plan_cost[S - 1] < plan_cost[best - 1]) best = S;
+      const int64_t n = (int64_t)p.B * p.groups * best;
+      const int P = plan_pieces[best - 1];
       p.plan[0] = best;
-      p.plan[1] = p.grid;  // the cluster count the choice assumed (diagnostics)
+      p.plan[1] = p.grid;
+      p.plan[2] = (int32_t)(P > 1 ? (n / p.grid) * p.grid : n);
+      p.plan[3] = P;
     }
   } else if (tid == 0) {
     p.plan[0] = p.splits;
     p.plan[1] = p.grid;
+    p.plan[2] = (int32_t)p.n_items;
+    p.plan[3] = 1;
   }
 
   // ancestor-or-self masks

@@ -14,6 +14,9 @@ Checked here:
     it chose (same kernels, same chunks) and matches the oracle;
   * the choice follows the lengths: equal B, H, Q pick different counts for
     a short and a long prefix;
+  * a pieced tail (S = 1, the last partial wave's items cut into pieces)
+    leaves every whole item's bytes as the explicit call's and matches the
+    oracle on the tail's rows;
   * the SIMT kernel keeps S_max.
 """
 import ctypes
@@ -43,13 +46,15 @@ def _gpu():
 
 
 def model_choice(prefix_lens, Q, H, s_max, grid):
+    """(S, P): the split count and the pieces per tail item (1: none)."""
     T = [-(-(int(P) + Q) // TK) for P in prefix_lens]
     B, rows = len(T), H * Q
     G = -(-rows // RG_TC)
-    best, best_ns = None, None
+    best = None
     for S in range(1, s_max + 1):
         load = [0] * grid
-        for i in range(B * G * S):
+        n = B * G * S
+        for i in range(n):
             bk = i // G
             k, b = bk % S, bk // S
             t = (k + 1) * T[b] // S - k * T[b] // S
@@ -57,10 +62,29 @@ def model_choice(prefix_lens, Q, H, s_max, grid):
                 load[i % grid] += ITEM_TILES + t
         ns = max(load) * TILE_NS
         if S > 1:
-            ns += B * rows * S * 512 * 4 // COMBINE_BYTES_PER_NS + COMBINE_NS
-        if best_ns is None or ns < best_ns:
-            best, best_ns = S, ns
-    return best
+            ns += B * S * rows * 512 * 4 // COMBINE_BYTES_PER_NS + COMBINE_NS
+        cand = (ns, S, 1)
+        full = (n // grid) * grid
+        r = n - full
+        if S == 1 and full > 0 and r > 0 and grid // r >= 2:
+            # the last r items cut into P pieces, one per otherwise idle cluster
+            P = grid // r
+            load = [0] * grid
+            for i in range(full):
+                if T[i // G] > 0:
+                    load[i % grid] += ITEM_TILES + T[i // G]
+            for v in range(r * P):
+                Tb = T[(full + v // P) // G]
+                q = v % P
+                t = (q + 1) * Tb // P - q * Tb // P
+                if t > 0:
+                    load[v] += ITEM_TILES + t
+            tns = max(load) * TILE_NS + r * P * RG_TC * 512 * 4 // COMBINE_BYTES_PER_NS + COMBINE_NS
+            if tns < ns:
+                cand = (tns, S, P)
+        if best is None or cand[0] < best[0]:
+            best = cand
+    return best[1], best[2]
 
 
 def ws_size(di, splits, algo):
@@ -77,11 +101,13 @@ def s_max_of(di, algo):
 
 
 def auto_call(di, algo="tc"):
+    """(out, lse, S used, grid the plan assumed, first tail item, pieces per
+    tail item) -- the plan words follow S at workspace offset 256."""
     ws = api.alloc_workspace(ws_size(di, 0, algo))
     out, lse = api.verify_attn(di, num_splits=0, algo=algo, workspace=ws)
     used = api.splits_used(ws)
-    grid = int(ws[260:264].cpu().numpy().view(np.int32)[0])  # the cluster count the plan assumed
-    return out, lse, used, grid
+    words = ws[256:272].cpu().numpy().view(np.int32)
+    return out, lse, used, int(words[1]), int(words[2]), int(words[3])
 
 
 SHAPES = {
@@ -91,6 +117,8 @@ SHAPES = {
     "ragged4": (4, 64, 32, [100, 5000, 20000, 700], "scattered"),
     "many_heads_paged": (8, 128, 16, [2048, 1500, 3000, 64, 2048, 900, 2500, 2048], "paged"),
     "small_mid": (2, 64, 16, [300, 777], "scattered"),
+    # 80 items on 36 clusters: two whole waves and a tail of 8 items
+    "tail_split": (10, 128, 16, [2048] * 10, "paged"),
 }
 
 
@@ -110,27 +138,47 @@ def test_device_choice_equals_the_model(name):
     p = make(name)
     di = api.device_inputs(p)
     s_max = s_max_of(di, "tc")
-    out, lse, used, grid = auto_call(di)
+    out, lse, used, grid, tail, pieces = auto_call(di)
     assert 1 <= used <= s_max
     assert grid >= 1
-    assert used == model_choice(p.prefix_lens, p.Q, p.H, s_max, grid), (used, s_max, grid)
-    # the same bytes as the explicit count
+    want = model_choice(p.prefix_lens, p.Q, p.H, s_max, grid)
+    assert (used, pieces) == want, (used, pieces, s_max, grid)
+    n_items = p.B * (-(-p.H * p.Q // RG_TC)) * used
     ref_out, ref_lse = api.verify_attn(di, num_splits=used, algo="tc")
     torch.cuda.synchronize()
-    assert torch.equal(out, ref_out)
-    assert torch.equal(lse, ref_lse)
+    if pieces == 1:
+        # the same bytes as the explicit count
+        assert tail == n_items
+        assert torch.equal(out, ref_out)
+        assert torch.equal(lse, ref_lse)
+    else:
+        # whole items give the explicit call's bytes; the rows of the pieced
+        # tail are merged from pieces (compared with the oracle elsewhere)
+        assert tail == (n_items // grid) * grid and 0 < n_items - tail < grid
+        G = -(-p.H * p.Q // RG_TC)
+        whole = np.ones((p.B, p.Q * p.H), dtype=bool)
+        for item in range(tail, n_items):
+            b, g = item // G, item % G
+            whole[b, g * RG_TC:(g + 1) * RG_TC] = False
+        m = torch.as_tensor(whole.reshape(p.B, p.Q, p.H), device=out.device)
+        assert torch.equal(out[m], ref_out[m])
+        assert torch.equal(lse[m], ref_lse[m])
+        assert not bool(m.all())
 
 
-@pytest.mark.parametrize("name", ["ragged4", "small_mid", "many_heads_paged"])
+@pytest.mark.parametrize("name", ["ragged4", "small_mid", "many_heads_paged", "tail_split"])
 def test_automatic_count_matches_oracle(name):
     p = make(name, seed=62)
     di = api.device_inputs(p)
-    out, lse, used, _ = auto_call(di)
+    out, lse, used, _, _, pieces = auto_call(di)
     rows = I.sample_rows(p, 2, seed=5) if name != "small_mid" else I.all_rows(p)
+    if name == "tail_split":
+        assert pieces > 1
+        rows = rows[rows[:, 0] == p.B - 1]  # the last sequence's row groups are the tail
     ro, rl = PT.oracle_rows(p, rows)
     go, gl = PT.gather_rows(out, lse, rows)
-    PT.assert_close(go, ro, "bf16", f"{name} auto S={used} out")
-    PT.assert_close(gl, rl, "bf16", f"{name} auto S={used} lse")
+    PT.assert_close(go, ro, "bf16", f"{name} auto S={used} P={pieces} out")
+    PT.assert_close(gl, rl, "bf16", f"{name} auto S={used} P={pieces} lse")
 
 
 def test_choice_follows_the_lengths():
@@ -142,15 +190,16 @@ def test_choice_follows_the_lengths():
                                              seed=64, layout="scattered", pool_slots=131072))
     s_max = s_max_of(short, "tc")
     assert s_max_of(long_, "tc") == s_max
-    _, _, s_short, grid = auto_call(short)
-    _, _, s_long, _ = auto_call(long_)
-    assert s_short == model_choice([4096], 64, 64, s_max, grid)
-    assert s_long == model_choice([100000], 64, 64, s_max, grid)
+    _, _, s_short, grid, _, _ = auto_call(short)
+    _, _, s_long, _, _, _ = auto_call(long_)
+    assert s_short == model_choice([4096], 64, 64, s_max, grid)[0]
+    assert s_long == model_choice([100000], 64, 64, s_max, grid)[0]
     assert s_short < s_long
 
 
 def test_simt_keeps_the_wave_count():
     p = make("small_mid", seed=65)
     di = api.device_inputs(p)
-    _, _, used, _ = auto_call(di, algo="simt")
+    _, _, used, _, tail, pieces = auto_call(di, algo="simt")
     assert used == s_max_of(di, "simt")
+    assert pieces == 1
