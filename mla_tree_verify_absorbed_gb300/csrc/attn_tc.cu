@@ -681,28 +681,35 @@ __device__ void value_rows(const Params& p, const Split sc, Ctl* c, uint32_t ran
     const float lse = l > 0.f ? (m + log2f(l)) * ln2 : -INFINITY;
     const int64_t orow = (int64_t)it.b * p.rows + row;
     if (slot < 0) {
-      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDl);
+      // bf16 row segments: 32-byte stores (whole sectors) when the caller's
+      // array allows them, else 16-byte ones
+      uint32_t* dst = reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDl + col0);
+      const bool wide = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
 #pragma unroll 1
       for (int c0 = 0; c0 < 256; c0 += 32) {
         uint32_t u[32];
         __syncwarp();
         tmem_ld32_sync(tO + c0, u);
         if (live) {
+          uint32_t w[16];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 o;
-            o.x = pack_bf16(__uint_as_float(u[8 * v + 0]) * inv, __uint_as_float(u[8 * v + 1]) * inv);
-            o.y = pack_bf16(__uint_as_float(u[8 * v + 2]) * inv, __uint_as_float(u[8 * v + 3]) * inv);
-            o.z = pack_bf16(__uint_as_float(u[8 * v + 4]) * inv, __uint_as_float(u[8 * v + 5]) * inv);
-            o.w = pack_bf16(__uint_as_float(u[8 * v + 6]) * inv, __uint_as_float(u[8 * v + 7]) * inv);
-            dst[(col0 + c0) / 8 + v] = o;
+          for (int v = 0; v < 16; ++v)
+            w[v] = pack_bf16(__uint_as_float(u[2 * v]) * inv, __uint_as_float(u[2 * v + 1]) * inv);
+          if (wide) {
+            st_global_v8(dst + c0 / 2, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+            st_global_v8(dst + c0 / 2 + 8, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+          } else {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              reinterpret_cast<uint4*>(dst + c0 / 2)[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
           }
         }
       }
       if (live && p.lse && h == 0) p.lse[orow] = lse;
     } else {
       const int64_t prow = slot * kRG + half * kRC + r;
-      float4* dst = reinterpret_cast<float4*>(p.part_o + prow * kDl);
+      // whole 32-byte sectors of the row (the workspace is 256-byte aligned)
+      float* dst = p.part_o + prow * kDl + col0;
 #pragma unroll 1
       for (int c0 = 0; c0 < 256; c0 += 32) {
         uint32_t u[32];
@@ -710,9 +717,11 @@ __device__ void value_rows(const Params& p, const Split sc, Ctl* c, uint32_t ran
         tmem_ld32_sync(tO + c0, u);
         if (live) {
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[(col0 + c0) / 4 + v] = make_float4(__uint_as_float(u[4 * v + 0]) * inv, __uint_as_float(u[4 * v + 1]) * inv,
-                                          __uint_as_float(u[4 * v + 2]) * inv, __uint_as_float(u[4 * v + 3]) * inv);
+          for (int v = 0; v < 4; ++v)
+            st_global_v8(dst + c0 + 8 * v, __uint_as_float(u[8 * v + 0]) * inv, __uint_as_float(u[8 * v + 1]) * inv,
+                         __uint_as_float(u[8 * v + 2]) * inv, __uint_as_float(u[8 * v + 3]) * inv,
+                         __uint_as_float(u[8 * v + 4]) * inv, __uint_as_float(u[8 * v + 5]) * inv,
+                         __uint_as_float(u[8 * v + 6]) * inv, __uint_as_float(u[8 * v + 7]) * inv);
         }
       }
       if (live && h == 0) p.part_lse[prow] = lse;

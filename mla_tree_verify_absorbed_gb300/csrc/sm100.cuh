@@ -131,6 +131,24 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ---------------------------------------------------------------------------
+// wide stores
+// ---------------------------------------------------------------------------
+// One 32-byte store (a whole L2 sector) of eight 32-bit words; ptr 32-byte
+// aligned.
+__device__ __forceinline__ void st_global_v8(float* ptr, float a0, float a1, float a2, float a3, float a4, float a5,
+                                             float a6, float a7) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "f"(a0), "f"(a1), "f"(a2),
+               "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7)
+               : "memory");
+}
+__device__ __forceinline__ void st_global_v8(uint32_t* ptr, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t a4, uint32_t a5, uint32_t a6, uint32_t a7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(a0), "r"(a1), "r"(a2),
+               "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // asynchronous copies
 // ---------------------------------------------------------------------------
 // 16-byte asynchronous global -> shared copy (L2 only), and the mbarrier

@@ -113,6 +113,24 @@ def test_split_invariance(algo):
         assert np.abs(gl - results[0][1]).max() <= 1e-4 * np.abs(results[0][1]).max() + 1e-5
 
 
+@pytest.mark.parametrize("num_splits", [1, 2])
+def test_output_16_byte_aligned_only(num_splits):
+    # the API asks for 16-byte aligned outputs; the tensor-core kernel writes
+    # whole 32-byte sectors only where the array allows them, so an output 16
+    # bytes past a 32-byte boundary takes the narrow stores: same bytes
+    p = mid_problem(27)
+    di = api.device_inputs(p)
+    ref_out, ref_lse = api.verify_attn(di, num_splits=num_splits, algo="tc")
+    n = p.B * p.Q * p.H * 512
+    buf = torch.empty(n + 8, dtype=torch.bfloat16, device="cuda")
+    out = buf[8:].view(p.B, p.Q, p.H, 512)
+    assert out.data_ptr() % 32 == 16
+    out, lse = api.verify_attn(di, out=out, num_splits=num_splits, algo="tc")
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out)
+    assert torch.equal(lse, ref_lse)
+
+
 @pytest.mark.parametrize("algo", ALGOS_BF16)
 def test_needles(algo):
     p = mid_problem(25)
