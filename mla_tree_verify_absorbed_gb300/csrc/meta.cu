@@ -53,6 +53,7 @@ __device__ int64_t block_inclusive_scan(int64_t v, int64_t* sh) {
 // into the warp's per-cluster totals in shared memory.
 constexpr int kPlanMaxClusters = 64;
 constexpr int kPlanMaxSplits = 64;
+constexpr int kPlanSharedSeqs = 2048;  // tile counts kept in shared memory for the plan
 constexpr unsigned long long kPlanUnitTiles = 14;
 constexpr int64_t kPlanTileNs = 1000;
 constexpr int64_t kPlanCombineBytesPerNs = 3000;
@@ -72,9 +73,12 @@ __device__ __forceinline__ int64_t plan_makespan_ns(const unsigned long long* ld
   return (int64_t)mx * kPlanTileNs;
 }
 
-// cost[S - 1] and pieces[S - 1] (1: no split tail) for S in [1, S_max].
-__device__ void plan_scores(const Params& p, unsigned long long* load, int64_t* cost, int* pieces) {
+// cost[S - 1] and pieces[S - 1] (1: no split tail) for S in [1, S_max];
+// tiles_sh holds T_b for b < kPlanSharedSeqs.
+__device__ void plan_scores(const Params& p, const int32_t* tiles_sh, unsigned long long* load, int64_t* cost,
+                            int* pieces) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  auto tiles = [&](int64_t b) -> int64_t { return b < kPlanSharedSeqs ? tiles_sh[b] : p.seq_tiles[b]; };
   const int C = p.grid;
   unsigned long long* ld = load + warp * kPlanMaxClusters;
   const int64_t rows_bytes = (int64_t)p.rows * (kDl * 4);  // fp32 partial bytes of one sequence's rows
@@ -85,7 +89,7 @@ __device__ void plan_scores(const Params& p, unsigned long long* load, int64_t* 
     for (int64_t i = lane; i < n; i += 32) {
       const int64_t bk = i / p.groups;
       const int64_t k = bk % S;
-      const int64_t T = p.seq_tiles[bk / S];
+      const int64_t T = tiles(bk / S);
       const int64_t t = ((k + 1) * T) / S - (k * T) / S;
       if (t > 0) atomicAdd(&ld[i % C], kPlanUnitTiles + (unsigned long long)t);
     }
@@ -100,11 +104,11 @@ __device__ void plan_scores(const Params& p, unsigned long long* load, int64_t* 
       for (int c = lane; c < C; c += 32) ld[c] = 0ull;
       __syncwarp();
       for (int64_t i = lane; i < full; i += 32) {
-        const int64_t T = p.seq_tiles[i / p.groups];
+        const int64_t T = tiles(i / p.groups);
         if (T > 0) atomicAdd(&ld[i % C], kPlanUnitTiles + (unsigned long long)T);
       }
       for (int64_t v = lane; v < r * P; v += 32) {
-        const int64_t T = p.seq_tiles[(full + v / P) / p.groups];
+        const int64_t T = tiles((full + v / P) / p.groups);
         const int64_t q = v % P;
         const int64_t t = ((q + 1) * T) / P - (q * T) / P;
         if (t > 0) atomicAdd(&ld[v], kPlanUnitTiles + (unsigned long long)t);
@@ -134,6 +138,7 @@ __global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
   __shared__ unsigned long long plan_load[(kMetaThreads / 32) * kPlanMaxClusters];
   __shared__ int64_t plan_cost[kPlanMaxSplits];
   __shared__ int plan_pieces[kPlanMaxSplits];
+  __shared__ int32_t tiles_sh[kPlanSharedSeqs];
   const int tid = threadIdx.x;
   grid_dep_launch();  // the slot pass may start launching; it waits for this kernel
   if (tid == 0) {
@@ -163,6 +168,7 @@ __global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
       if (e) set_err(p.err, e);
       const int64_t T = (N + p.tk - 1) / p.tk;
       p.seq_tiles[b] = (int32_t)T;
+      if (b < kPlanSharedSeqs) tiles_sh[b] = (int32_t)T;
       nkv = N;
     }
     const int64_t k_inc = block_inclusive_scan(nkv, sh);
@@ -181,7 +187,7 @@ __global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
   // item of a tail cut into pieces, pieces per tail item
   if (p.auto_plan && p.splits >= 1 && p.splits <= kPlanMaxSplits && p.grid >= 1 &&
       p.grid <= kPlanMaxClusters && p.part_slots >= p.grid) {
-    plan_scores(p, plan_load, plan_cost, plan_pieces);
+    plan_scores(p, tiles_sh, plan_load, plan_cost, plan_pieces);
     __syncthreads();
     if (tid == 0) {
       int best = 1;

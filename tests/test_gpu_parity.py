@@ -95,13 +95,24 @@ def test_tiny_fp32_via_simt_bf16_shape():
         check_all_rows(p, out, lse, f"tiny_bf16/{algo}")
 
 
+def ragged_batch_problem(seed=28):
+    # four sequences of very different lengths (1 to 40 tiles): chunks of
+    # one split count differ in size between sequences, some are empty
+    return I.make_problem(name="ragged_batch", dtype="bf16", B=4, H=64, Q=16, prefix_lens=[2500, 0, 700, 33],
+                          seed=seed, layout="scattered", pool_slots=4096)
+
+
 @pytest.mark.parametrize("algo", ALGOS_BF16)
-def test_split_invariance(algo):
-    p = mid_problem(24)
+@pytest.mark.parametrize("maker", [mid_problem, ragged_batch_problem], ids=["mid", "ragged_batch"])
+def test_split_invariance(algo, maker):
+    p = maker(24)
     rows = I.all_rows(p)
     ro, rl = PT.oracle_rows(p, rows)
     results = []
-    for ns in (1, 2, 7, 0):
+    # 20 and 40 chunks: more chunks than most sequences have tiles (empty
+    # chunks), the combine's four-warps-per-row form, and (40) more than 32
+    # pieces per row
+    for ns in (1, 2, 7, 20, 40, 0):
         _, out, lse = run(p, algo=algo, num_splits=ns)
         go, gl = PT.gather_rows(out, lse, rows)
         PT.assert_close(go, ro, "bf16", f"splits={ns} out")
