@@ -53,68 +53,82 @@ __device__ int64_t block_inclusive_scan(int64_t v, int64_t* sh) {
 // into the warp's per-cluster totals in shared memory.
 constexpr int kPlanMaxClusters = 64;
 constexpr int kPlanMaxSplits = 64;
-constexpr int kPlanSharedSeqs = 2048;  // tile counts kept in shared memory for the plan
-constexpr unsigned long long kPlanUnitTiles = 14;
+constexpr int kPlanSharedSeqs = 2048;  // the plan is made for batches whose tile counts fit shared memory
+constexpr uint32_t kPlanUnitTiles = 14;
 constexpr int64_t kPlanTileNs = 1000;
 constexpr int64_t kPlanCombineBytesPerNs = 3000;
 constexpr int64_t kPlanCombineFixedNs = 3000;
 
-// The warp's largest per-cluster total, in ns.
-__device__ __forceinline__ int64_t plan_makespan_ns(const unsigned long long* ld, int C) {
+// Tiles of chunk k when T tiles are cut into n chunks: floor((k+1) T / n) -
+// floor(k T / n), in 32-bit arithmetic (T = q n + rem, rem < n <= 4096).
+__device__ __forceinline__ uint32_t plan_chunk_tiles(uint32_t T, uint32_t n, uint32_t k) {
+  const uint32_t q = T / n, rem = T - q * n;
+  return q + ((k + 1) * rem) / n - (k * rem) / n;
+}
+
+// The warp's largest per-cluster total, in ns.  Totals are 32-bit tile counts:
+// one that wrapped could only make the plan slower, never wrong, since every
+// plan computes the same attention.
+__device__ __forceinline__ int64_t plan_makespan_ns(const uint32_t* ld, int C) {
   const int lane = threadIdx.x & 31;
   __syncwarp();
-  unsigned long long mx = 0ull;
-  for (int c = lane; c < C; c += 32) mx = ld[c] > mx ? ld[c] : mx;
+  uint32_t mx = 0u;
+  for (int c = lane; c < C; c += 32) mx = max(mx, ld[c]);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long v = __shfl_xor_sync(0xffffffffu, mx, o);
-    mx = v > mx ? v : mx;
-  }
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   return (int64_t)mx * kPlanTileNs;
 }
 
 // cost[S - 1] and pieces[S - 1] (1: no split tail) for S in [1, S_max];
-// tiles_sh holds T_b for b < kPlanSharedSeqs.
-__device__ void plan_scores(const Params& p, const int32_t* tiles_sh, unsigned long long* load, int64_t* cost,
-                            int* pieces) {
+// tiles_sh holds every T_b (B <= kPlanSharedSeqs).  Item counts are below
+// 2^26 (the host refuses larger plans), so unit indices fit 32 bits.
+__device__ void plan_scores(const Params& p, const int32_t* tiles_sh, uint32_t* load, int64_t* cost, int* pieces) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  auto tiles = [&](int64_t b) -> int64_t { return b < kPlanSharedSeqs ? tiles_sh[b] : p.seq_tiles[b]; };
-  const int C = p.grid;
-  unsigned long long* ld = load + warp * kPlanMaxClusters;
+  auto tiles = [&](int b) -> uint32_t { return (uint32_t)tiles_sh[b]; };
+  const int C = p.grid, G = p.groups;
+  uint32_t* ld = load + warp * kPlanMaxClusters;
   const int64_t rows_bytes = (int64_t)p.rows * (kDl * 4);  // fp32 partial bytes of one sequence's rows
   for (int S = warp + 1; S <= p.splits; S += kMetaThreads / 32) {
-    for (int c = lane; c < C; c += 32) ld[c] = 0ull;
+    for (int c = lane; c < C; c += 32) ld[c] = 0u;
     __syncwarp();
-    const int64_t n = (int64_t)p.B * p.groups * S;
-    for (int64_t i = lane; i < n; i += 32) {
-      const int64_t bk = i / p.groups;
-      const int64_t k = bk % S;
-      const int64_t T = tiles(bk / S);
-      const int64_t t = ((k + 1) * T) / S - (k * T) / S;
-      if (t > 0) atomicAdd(&ld[i % C], kPlanUnitTiles + (unsigned long long)t);
+    const int n = p.B * G * S;
+    // chunk bk = b S + k: its G items are units bk G .. bk G + G - 1, dealt
+    // to consecutive clusters from (bk G) mod C
+    for (int bk = lane; bk < p.B * S; bk += 32) {
+      const int b = bk / S;
+      const uint32_t t = plan_chunk_tiles(tiles(b), (uint32_t)S, (uint32_t)(bk - b * S));
+      if (t == 0) continue;
+      int c = (int)(((int64_t)bk * G) % C);
+      for (int g = 0; g < G; ++g) {
+        atomicAdd(&ld[c], kPlanUnitTiles + t);
+        if (++c == C) c = 0;
+      }
     }
     int64_t best = plan_makespan_ns(ld, C);
     if (S > 1) best += (int64_t)p.B * S * rows_bytes / kPlanCombineBytesPerNs + kPlanCombineFixedNs;
     int best_p = 1;
-    const int64_t full = (n / C) * C, r = n - full;
+    const int full = (n / C) * C, r = n - full;
     if (S == 1 && full > 0 && r > 0 && C / r >= 2) {
       // the same items, the last r cut into P pieces each
-      const int P = (int)(C / r);
+      const int P = C / r;
       __syncwarp();
-      for (int c = lane; c < C; c += 32) ld[c] = 0ull;
+      for (int c = lane; c < C; c += 32) ld[c] = 0u;
       __syncwarp();
-      for (int64_t i = lane; i < full; i += 32) {
-        const int64_t T = tiles(i / p.groups);
-        if (T > 0) atomicAdd(&ld[i % C], kPlanUnitTiles + (unsigned long long)T);
+      for (int b = lane; b * G < full; b += 32) {
+        const uint32_t T = tiles(b);
+        if (T == 0) continue;
+        int c = (int)(((int64_t)b * G) % C);
+        for (int g = 0; g < G && b * G + g < full; ++g) {
+          atomicAdd(&ld[c], kPlanUnitTiles + T);
+          if (++c == C) c = 0;
+        }
       }
-      for (int64_t v = lane; v < r * P; v += 32) {
-        const int64_t T = tiles((full + v / P) / p.groups);
-        const int64_t q = v % P;
-        const int64_t t = ((q + 1) * T) / P - (q * T) / P;
-        if (t > 0) atomicAdd(&ld[v], kPlanUnitTiles + (unsigned long long)t);
+      for (int v = lane; v < r * P; v += 32) {
+        const uint32_t t = plan_chunk_tiles(tiles((full + v / P) / G), (uint32_t)P, (uint32_t)(v % P));
+        if (t > 0) atomicAdd(&ld[v], kPlanUnitTiles + t);
       }
       const int64_t ns = plan_makespan_ns(ld, C) +
-                         r * P * (int64_t)p.rg * (kDl * 4) / kPlanCombineBytesPerNs + kPlanCombineFixedNs;
+                         (int64_t)r * P * p.rg * (kDl * 4) / kPlanCombineBytesPerNs + kPlanCombineFixedNs;
       if (ns < best) {
         best = ns;
         best_p = P;
@@ -135,7 +149,7 @@ __device__ void plan_scores(const Params& p, const int32_t* tiles_sh, unsigned l
 __global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
   __shared__ int64_t sh[kMetaThreads];
   __shared__ int64_t carry_kv;
-  __shared__ unsigned long long plan_load[(kMetaThreads / 32) * kPlanMaxClusters];
+  __shared__ uint32_t plan_load[(kMetaThreads / 32) * kPlanMaxClusters];
   __shared__ int64_t plan_cost[kPlanMaxSplits];
   __shared__ int plan_pieces[kPlanMaxSplits];
   __shared__ int32_t tiles_sh[kPlanSharedSeqs];
@@ -185,20 +199,39 @@ __global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
   // the work split of this call (the tile counts above are visible to the
   // whole block after the loop's last barrier): S, the grid assumed, the first
   // item of a tail cut into pieces, pieces per tail item
-  if (p.auto_plan && p.splits >= 1 && p.splits <= kPlanMaxSplits && p.grid >= 1 &&
+  // (a batch of more than kPlanSharedSeqs sequences has far more row groups
+  // than clusters, where the wave-filling S_max is the plan)
+  if (p.auto_plan && p.B <= kPlanSharedSeqs && p.splits >= 1 && p.splits <= kPlanMaxSplits && p.grid >= 1 &&
       p.grid <= kPlanMaxClusters && p.part_slots >= p.grid) {
     plan_scores(p, tiles_sh, plan_load, plan_cost, plan_pieces);
     __syncthreads();
-    if (tid == 0) {
-      int best = 1;
-      for (int S = 2; S <= p.splits; ++S)
-        if (plan_cost[S - 1] < plan_cost[best - 1]) best = S;
-      const int64_t n = (int64_t)p.B * p.groups * best;
-      const int P = plan_pieces[best - 1];
-      p.plan[0] = best;
-      p.plan[1] = p.grid;
-      p.plan[2] = (int32_t)(P > 1 ? (n / p.grid) * p.grid : n);
-      p.plan[3] = P;
+    if (tid < 32) {
+      // the cheapest S (the smaller on a tie): lane l looks at S = l + 1, l + 33
+      int64_t bc = INT64_MAX;
+      int bs = 0;
+      for (int S = tid + 1; S <= p.splits; S += 32)
+        if (plan_cost[S - 1] < bc) {
+          bc = plan_cost[S - 1];
+          bs = S;
+        }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const int64_t oc = __shfl_xor_sync(0xffffffffu, bc, o);
+        const int os = __shfl_xor_sync(0xffffffffu, bs, o);
+        if (oc < bc || (oc == bc && os < bs)) {
+          bc = oc;
+          bs = os;
+        }
+      }
+      if (tid == 0) {
+        const int best = bs;
+        const int64_t n = (int64_t)p.B * p.groups * best;
+        const int P = plan_pieces[best - 1];
+        p.plan[0] = best;
+        p.plan[1] = p.grid;
+        p.plan[2] = (int32_t)(P > 1 ? (n / p.grid) * p.grid : n);
+        p.plan[3] = P;
+      }
     }
   } else if (tid == 0) {
     p.plan[0] = p.splits;
