@@ -32,8 +32,10 @@
 // in flight.  P (bf16) and the per-row rescale factors of score CTA c are
 // staged in its own shared memory and moved to value CTA 2 + c by one thread
 // with a bulk shared::cta -> shared::cluster copy whose bytes complete that
-// CTA's barrier.  The value CTAs rescale their own O rows when a factor
-// differs from 1 and write the outputs.
+// CTA's barrier; the commit of the PV MMAs that read a P buffer arrives on
+// both score CTAs' barriers directly, so P buffers come back without a relay
+// thread.  The value CTAs rescale their own O rows when a factor differs from
+// 1 and write the outputs.
 //
 // Data movement.  Eight producer warps per CTA gather the CTA's share of every
 // tile with 16-byte cp.async copies written straight into the 128-byte
@@ -83,7 +85,7 @@ constexpr int kProducerThreads = 32 * kProducerWarps;
 // reaches TMEM lanes 32 (w % 4) ..); warpgroup h takes columns half h.
 constexpr int kWarpRows = 8, kRowWarps = 8, kRowThreads = 32 * kRowWarps;
 constexpr int kWarpMma = 16;  // MMA issue (even CTAs) or tile-landed relay (odd CTAs)
-constexpr int kWarpAux = 17;  // TMEM allocation; lane 0: P bulk copies (score CTAs), P release (value CTAs)
+constexpr int kWarpAux = 17;  // TMEM allocation; lane 0 of score CTAs: P bulk copies
 
 // score CTA stage: its 32 tokens x 576 columns, as 9 chunks of 64 columns
 // (chunks 0-7 kv_c, chunk 8 k_pe), each chunk 32 rows of 128 bytes
@@ -122,7 +124,7 @@ struct alignas(16) Ctl {
   uint64_t s_full[2];           // score: S tile in TMEM
   uint64_t s_free[2];           // score, rank 0: both CTAs' softmax warps loaded S (16 warp arrivals)
   uint64_t q_ready;             // score, rank 0: both CTAs' queries in TMEM (16 warp arrivals)
-  uint64_t p_free[2];           // score: the value partner finished with its P buffer
+  uint64_t p_free[2];           // score: the value pair's PV MMAs that read this P buffer completed (commit)
   uint64_t fin_free;            // score: the value partner consumed lfin/mfin (256 arrivals)
   uint64_t xch[2];              // score: both halves' partial row maxima of a tile written (8 warp arrivals)
   uint64_t xfin;                // score: half 1's partial row sums of an item written (4 warp arrivals)
@@ -149,11 +151,13 @@ static_assert(kOffPStage % 1024 == 0 && kOffAStage % 16 == 0, "staging buffers: 
 static_assert(kWarpRows % 4 == 0 && kRowWarps == 8, "the row warps must form two warpgroups (TMEM lane quadrants)");
 static_assert(kWarpAux < kThreads / 32, "warp roles exceed the CTA");
 
-// Wait sites, recorded in the workspace's second error word when a wait gives up.
+// Wait sites, recorded in the workspace's second error word when a wait gives
+// up.  The numbers are part of the error report, so they stay fixed (13 was
+// the wait of a P-release thread the MMA commit has replaced).
 enum {
-  kSiteEmpty = 1, kSiteQReady, kSiteFullS, kSiteSFree, kSiteSFull, kSitePFree, kSiteFinFree,
-  kSiteFullV, kSiteOReady, kSitePFull, kSitePvPrev, kSitePvLast, kSiteRelease, kSiteRelay, kSiteFinFull,
-  kSiteXch, kSitePStaged, kSiteHold
+  kSiteEmpty = 1, kSiteQReady = 2, kSiteFullS = 3, kSiteSFree = 4, kSiteSFull = 5, kSitePFree = 6,
+  kSiteFinFree = 7, kSiteFullV = 8, kSiteOReady = 9, kSitePFull = 10, kSitePvPrev = 11, kSitePvLast = 12,
+  kSiteRelay = 14, kSiteFinFull = 15, kSiteXch = 16, kSitePStaged = 17, kSiteHold = 18
 };
 
 // Bounded wait on a barrier of this CTA.  Barriers that other CTAs (or pair
@@ -599,6 +603,9 @@ __device__ void value_mma(const Params& p, const Split sc, uint8_t* smem, Ctl* c
         if (kk == 2) ready = (t + 1 < it.t1) && ready_test(j + 1);
       }
       mma_pair_commit_warp(&c->pv_done[pb], 0xC);
+      // the same completion frees both score CTAs' P buffers (and the local
+      // staging buffers their bulk copies read) without a relay
+      mma_pair_commit_warp(&c->p_free[pb], 0x3);
       mma_pair_commit_warp(&c->empty[s], 0xC);
     }
     return true;
@@ -609,19 +616,6 @@ __device__ void value_mma(const Params& p, const Split sc, uint8_t* smem, Ctl* c
     if ((threadIdx.x & 31) == 0) mbar_wait_drain(&c->drain, 0, kDrainLimitNs);
     __syncwarp();
   }
-}
-
-// Releases each tile's P buffer back to the score partner once the PV MMAs
-// that read it have completed (one thread).
-__device__ void value_release(const Params& p, const Split sc, Ctl* c, uint32_t rank, int cluster_id, int n_clusters) {
-  int j = 0;
-  for_items(p, sc, cluster_id, n_clusters, [&](int64_t, const Item& it) {
-    for (int t = it.t0; t < it.t1; ++t, ++j) {
-      if (!wait(&c->pv_done[j & 1], (uint32_t)(j >> 1) & 1u, c, kSiteRelease, j)) return false;
-      mbar_arrive_cluster_relaxed(&c->p_free[j & 1], rank - 2);
-    }
-    return true;
-  });
 }
 
 // Row warps of a value CTA (warpgroup h takes O columns [256 h, 256 h + 256)):
@@ -797,10 +791,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads,
     else if (score) score_mma(p, sc, smem, c, cluster_id, n_clusters);
     else value_mma(p, sc, smem, c, cluster_id, n_clusters);
   } else if (warp == kWarpAux) {
-    if ((threadIdx.x & 31) == 0) {
-      if (score) p_copier(p, sc, smem, c, rank, cluster_id, n_clusters);
-      else value_release(p, sc, c, rank, cluster_id, n_clusters);
-    }
+    if ((threadIdx.x & 31) == 0 && score) p_copier(p, sc, smem, c, rank, cluster_id, n_clusters);
   } else if (warp >= kWarpRows && warp < kWarpRows + kRowWarps) {
     if (score) score_softmax(p, sc, smem, c, rank, cluster_id, n_clusters);
     else value_rows(p, sc, c, rank, cluster_id, n_clusters);
