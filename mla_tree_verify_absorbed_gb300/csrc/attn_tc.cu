@@ -387,13 +387,38 @@ __device__ void score_mma(const Params& p, const Split sc, uint8_t* smem, Ctl* c
   }
 }
 
+// Stages query row `row` of sequence b into Tensor Memory for row thread
+// (quadrant of tQ, half h): columns [144 h, 144 h + 144), column c holding
+// elements 2c, 2c+1 of the 576 (512 latent, then 64 rope).
+__device__ __forceinline__ void stage_query_row(const Params& p, int b, int row, bool live, int h, uint32_t tQ) {
+  const uint4* ql = reinterpret_cast<const uint4*>(p.q_lat) + ((int64_t)b * p.rows + row) * (kDl / 8);
+  const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe) + ((int64_t)b * p.rows + row) * (kDr / 8);
+#pragma unroll 1
+  for (int c0 = 144 * h; c0 < 144 * h + 144; c0 += 16) {
+    uint32_t wv[16];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int col = c0 + 4 * v;  // 4 columns per 16-byte vector
+      uint4 x = make_uint4(0, 0, 0, 0);
+      if (live) x = col < 256 ? ql[col / 4] : qp[(col - 256) / 4];
+      wv[4 * v + 0] = x.x;
+      wv[4 * v + 1] = x.y;
+      wv[4 * v + 2] = x.z;
+      wv[4 * v + 3] = x.w;
+    }
+    __syncwarp();
+    tmem_st_32x32b_x16(tQ + c0, wv);
+  }
+  tmem_wait_st();
+}
+
 // Online softmax of this CTA's 128 rows.  Each row is shared by two threads
 // (warps w and w + 4 of the row warps) that take columns [32 h, 32 h + 32) of
 // every tile: they exchange partial maxima per tile through shared memory, so
 // both follow the same running max, and keep partial row sums that are added
 // once per item.
 __device__ void score_softmax(const Params& p, const Split sc, uint8_t* smem, Ctl* c, uint32_t rank, int cluster_id,
-                              int n_clusters) {
+                              int n_clusters, int pre_g) {
   const int lane = threadIdx.x & 31;
   const int w = (threadIdx.x >> 5) - kWarpRows;     // 0..7
   const int wq = w & 3;                              // TMEM lane quadrant of this warp
@@ -408,6 +433,7 @@ __device__ void score_softmax(const Params& p, const Split sc, uint8_t* smem, Ct
   const float sl2 = p.scale_log2;
   const int nq = p.Q;
   int j = 0, seg = 0;
+  bool first = true;
   for_items(p, sc, cluster_id, n_clusters, [&](int64_t, const Item& it) {
     const int b = it.b;
     const int row = it.g * kRG + (int)rank * kRC + r;
@@ -415,28 +441,11 @@ __device__ void score_softmax(const Params& p, const Split sc, uint8_t* smem, Ct
     const int64_t P = p.prefix_lens[b];
     const uint64_t anc = live ? p.anc[(int64_t)b * p.Q + row / p.H] : 0ull;
 
-    // stage this item's queries into TMEM (half h: columns [144 h, 144 h + 144));
-    // column c holds elements 2c, 2c+1
+    // stage this item's queries into TMEM (half h: columns [144 h, 144 h + 144)),
+    // unless they were staged before the wait on the metadata kernel
     {
-      const uint4* ql = reinterpret_cast<const uint4*>(p.q_lat) + ((int64_t)b * p.rows + row) * (kDl / 8);
-      const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe) + ((int64_t)b * p.rows + row) * (kDr / 8);
-#pragma unroll 1
-      for (int c0 = 144 * h; c0 < 144 * h + 144; c0 += 16) {
-        uint32_t wv[16];
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int col = c0 + 4 * v;  // 4 columns per 16-byte vector
-          uint4 x = make_uint4(0, 0, 0, 0);
-          if (live) x = col < 256 ? ql[col / 4] : qp[(col - 256) / 4];
-          wv[4 * v + 0] = x.x;
-          wv[4 * v + 1] = x.y;
-          wv[4 * v + 2] = x.z;
-          wv[4 * v + 3] = x.w;
-        }
-        __syncwarp();
-        tmem_st_32x32b_x16(tQ + c0, wv);
-      }
-      tmem_wait_st();
+      if (!(first && b == 0 && it.g == pre_g)) stage_query_row(p, b, row, live, h, tQ);
+      first = false;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster_relaxed(&c->q_ready, 0);
@@ -731,9 +740,10 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads,
   uint8_t* smem = smem_raw;
   const uint32_t rank = cluster_ctarank();
   const int warp = threadIdx.x >> 5;
-  // The prologue (barriers, Tensor Memory, cluster sync) touches only this
-  // cluster's shared and Tensor Memory, so it may overlap the end of the
-  // metadata kernel; everything after grid_dep_wait() reads its results.
+  // The prologue (barriers, Tensor Memory, cluster sync, and for one sequence
+  // the first item's queries) touches only this cluster's shared and Tensor
+  // Memory and caller inputs, so it may overlap the end of the metadata
+  // kernel; everything after grid_dep_wait() reads its results.
   Ctl* c = reinterpret_cast<Ctl*>(smem + kOffCtl);
   const bool leader = (rank & 1) == 0;
   if (threadIdx.x == 0) {
@@ -768,6 +778,17 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads,
   tc_fence_before();
   cluster_sync();  // barriers of all CTAs initialised before any remote use
   tc_fence_after();
+  // One sequence: a cluster's first work item has row group cluster mod G
+  // whatever split count the metadata kernel picks, and queries are caller
+  // inputs it does not write -- stage them while it runs.
+  int pre_g = -1;
+  if (p.B == 1 && rank < 2 && warp >= kWarpRows && warp < kWarpRows + kRowWarps) {
+    const int w = warp - kWarpRows;
+    const int r = (w & 3) * 32 + (threadIdx.x & 31);
+    pre_g = (int)((blockIdx.x / kClusterCtas) % p.groups);
+    const int row = pre_g * kRG + (int)rank * kRC + r;
+    stage_query_row(p, 0, row, row < p.rows, w >> 2, c->tmem_base + 128 + ((uint32_t)((w & 3) * 32) << 16));
+  }
   grid_dep_wait();
   // All CTAs of a cluster take the same branch here.  The validation bits are
   // final once the metadata kernel has completed; the timeout bit may be
@@ -793,7 +814,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads,
   } else if (warp == kWarpAux) {
     if ((threadIdx.x & 31) == 0 && score) p_copier(p, sc, smem, c, rank, cluster_id, n_clusters);
   } else if (warp >= kWarpRows && warp < kWarpRows + kRowWarps) {
-    if (score) score_softmax(p, sc, smem, c, rank, cluster_id, n_clusters);
+    if (score) score_softmax(p, sc, smem, c, rank, cluster_id, n_clusters, pre_g);
     else value_rows(p, sc, c, rank, cluster_id, n_clusters);
   }
 

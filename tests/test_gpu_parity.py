@@ -124,6 +124,17 @@ def test_split_invariance(algo, maker):
         assert np.abs(gl - results[0][1]).max() <= 1e-4 * np.abs(results[0][1]).max() + 1e-5
 
 
+@pytest.mark.parametrize("num_splits", [9, 7, 0])
+def test_one_sequence_with_empty_leading_chunks(num_splits):
+    # one sequence of 5 tiles (16 row groups): cut 9 ways, chunk 0 is empty,
+    # so a cluster's first real work item is not the row group whose queries
+    # it staged while the metadata kernel ran -- it must stage them again
+    p = I.make_problem(name="one_seq_short", dtype="bf16", B=1, H=64, Q=64, prefix_lens=[256], seed=29,
+                       layout="scattered", pool_slots=1024)
+    _, out, lse = run(p, algo="tc", num_splits=num_splits)
+    check_all_rows(p, out, lse, f"one short sequence, splits={num_splits}")
+
+
 @pytest.mark.parametrize("num_splits", [1, 2])
 def test_output_16_byte_aligned_only(num_splits):
     # the API asks for 16-byte aligned outputs; the tensor-core kernel writes
