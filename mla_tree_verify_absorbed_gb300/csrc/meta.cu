@@ -15,20 +15,33 @@
 namespace mlav {
 
 constexpr int kMetaThreads = 1024;
+static_assert(kMetaThreads / 32 == 32, "the block scan combines 32 warp totals in one warp");
 
-// Block-wide inclusive scan of one value per thread (kMetaThreads threads).
+// Block-wide inclusive scan of one value per thread (kMetaThreads threads):
+// a shuffle scan inside each warp, then one warp scans the 32 warp totals --
+// two block barriers instead of one pair per doubling step.  sh holds at
+// least kMetaThreads / 32 entries.
 __device__ int64_t block_inclusive_scan(int64_t v, int64_t* sh) {
-  const int tid = threadIdx.x;
-  sh[tid] = v;
-  __syncthreads();
-  for (int off = 1; off < kMetaThreads; off <<= 1) {
-    int64_t add = (tid >= off) ? sh[tid - off] : 0;
-    __syncthreads();
-    sh[tid] += add;
-    __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
   }
-  int64_t r = sh[tid];
+  if (lane == 31) sh[warp] = v;
   __syncthreads();
+  if (warp == 0) {
+    int64_t t = sh[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t u = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += u;
+    }
+    sh[lane] = t;  // inclusive prefix over the warps
+  }
+  __syncthreads();
+  const int64_t r = v + (warp > 0 ? sh[warp - 1] : 0);
+  __syncthreads();  // sh may be reused by the caller's next round
   return r;
 }
 
@@ -147,7 +160,7 @@ __device__ void plan_scores(const Params& p, const int32_t* tiles_sh, uint32_t* 
 // seq_kv_base of N_b (a thread per sequence), fixes the call's split count,
 // then validates the parents and builds anc (a thread per node).
 __global__ void __launch_bounds__(kMetaThreads) meta_seq_kernel(Params p) {
-  __shared__ int64_t sh[kMetaThreads];
+  __shared__ int64_t sh[kMetaThreads / 32];
   __shared__ int64_t carry_kv;
   __shared__ uint32_t plan_load[(kMetaThreads / 32) * kPlanMaxClusters];
   __shared__ int64_t plan_cost[kPlanMaxSplits];
