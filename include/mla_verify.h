@@ -193,7 +193,10 @@ mla_status mla_verify_check(const void *workspace, mla_stream_t stream, uint32_t
 
 /* Synchronises `stream`, then reads the split count (KV chunks per row group)
  * that the last mla_verify_attn call on this workspace used: num_splits when
- * that was > 0, else the one the library chose.  Debug and benchmark aid; no
+ * that was > 0, else the one the library chose (a call with B or Q zero
+ * launches nothing and leaves the value unchanged).  Returns
+ * MLA_ERR_WORKSPACE for a NULL workspace and MLA_ERR_INVALID_ARG for a NULL
+ * `splits`, before touching the device.  Debug and benchmark aid; no
  * counterpart on the pages. */
 mla_status mla_verify_splits_used(const void *workspace, mla_stream_t stream, int32_t *splits);
 

@@ -136,6 +136,14 @@ def test_workspace_checks(lib):
     assert lib.mla_verify_workspace_size(ctypes.byref(a), 5000) == 0
 
 
+def test_splits_used_argument_checks(lib):
+    # both checks come before any CUDA call
+    v = ctypes.c_int32(-7)
+    assert lib.mla_verify_splits_used(None, None, ctypes.byref(v)) == api.MLA_ERR_WORKSPACE
+    assert lib.mla_verify_splits_used(ctypes.c_void_p(0x100000), None, None) == api.MLA_ERR_INVALID_ARG
+    assert v.value == -7
+
+
 def test_build_meta_validation(lib):
     a = fake_args()
     st = lib.mla_verify_build_meta(ctypes.byref(a), ctypes.c_void_p(0x100000), ctypes.c_size_t(1 << 40),
