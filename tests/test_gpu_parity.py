@@ -154,6 +154,21 @@ def test_output_16_byte_aligned_only(num_splits):
 
 
 @pytest.mark.parametrize("algo", ALGOS_BF16)
+@pytest.mark.parametrize("page_size,H,Q,lens", [
+    (8, 16, 13, [500, 9, 1200]),        # 208 rows: one ragged row group per sequence
+    (32, 24, 5, [0, 700]),              # 120 rows, an empty prefix
+    (128, 128, 1, [900, 2000, 31]),     # 128 heads, one node, pages wider than a tile
+    (32, 16, 64, [300]),                # 1024 rows, a 64-node tree over a short prefix
+], ids=["p8_H16_Q13", "p32_H24_Q5", "p128_H128_Q1", "p32_H16_Q64"])
+def test_page_sizes_and_head_counts(algo, page_size, H, Q, lens):
+    n_pages = sum(-(-(int(P) + Q) // page_size) for P in lens) + 3
+    p = I.make_problem(name="pages_heads", dtype="bf16", B=len(lens), H=H, Q=Q, prefix_lens=lens, seed=30,
+                       layout="paged", page_size=page_size, n_pages=n_pages)
+    _, out, lse = run(p, algo=algo)
+    check_all_rows(p, out, lse, f"page {page_size} H {H} Q {Q}")
+
+
+@pytest.mark.parametrize("algo", ALGOS_BF16)
 def test_needles(algo):
     p = mid_problem(25)
     I.plant_needles(p, seed=5)
