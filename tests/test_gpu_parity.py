@@ -169,6 +169,33 @@ def test_page_sizes_and_head_counts(algo, page_size, H, Q, lens):
 
 
 @pytest.mark.parametrize("algo", ALGOS_BF16)
+def test_padded_pool_rows(algo):
+    # the cache rows inside a wider array: kv_c at columns [0, 512), k_pe at
+    # [640, 704) of 704-element rows -- the gathers follow the row strides, so
+    # the results are the packed pool's bytes, and the compaction copies the
+    # same rows
+    import dataclasses
+    p = mid_problem(31)
+    di = api.device_inputs(p)
+    ref_out, ref_lse = api.verify_attn(di, algo=algo, num_splits=3)
+    wide = torch.zeros((di.pool.shape[0], 704), dtype=di.pool.dtype, device=di.pool.device)
+    wide[:, :512] = di.pool[:, :512]
+    wide[:, 640:704] = di.pool[:, 512:576]
+    dw = dataclasses.replace(di, kv_c=wide[:, :512], k_pe=wide[:, 640:704], pool=None)
+    out, lse = api.verify_attn(dw, algo=algo, num_splits=3)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out)
+    assert torch.equal(lse, ref_lse)
+    total = int(np.sum(np.asarray(p.prefix_lens, dtype=np.int64) + p.Q))
+    d_ref = torch.empty((total, 576), dtype=di.pool.dtype, device=di.pool.device)
+    d_wide = torch.empty_like(d_ref)
+    api.kv_compact(di, d_ref)
+    api.kv_compact(dw, d_wide)
+    torch.cuda.synchronize()
+    assert torch.equal(d_ref, d_wide)
+
+
+@pytest.mark.parametrize("algo", ALGOS_BF16)
 def test_needles(algo):
     p = mid_problem(25)
     I.plant_needles(p, seed=5)
