@@ -102,7 +102,7 @@ typedef struct {
     int max_pages;              /* columns of block_table */
     const int32_t *prefix_lens; /* [B], >= 0 */
     const int32_t *tree_parent; /* [B][Q], parent[i] in [-1, i-1]; -1 hangs off the prefix */
-    float scale;                /* score scale, e.g. 1/sqrt(192) */
+    float scale;                /* score scale, finite and > 0, e.g. 1/sqrt(192) */
     void *out;                  /* [B][Q][H][512] of dtype */
     float *lse;                 /* [B][Q][H], natural log; may be NULL */
     mla_algo algo;              /* kernel family, see mla_algo */

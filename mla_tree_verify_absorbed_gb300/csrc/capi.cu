@@ -93,7 +93,10 @@ mla_status validate_call(const mla_verify_args* a) {
   if (!aligned16(a->q_lat) || !aligned16(a->q_pe) || !aligned16(a->kv_c) || !aligned16(a->k_pe) ||
       !aligned16(a->out))
     return MLA_ERR_INVALID_ARG;
-  if (!std::isfinite(a->scale)) return MLA_ERR_INVALID_ARG;
+  // the kernels take the running maximum on raw scores and scale it after,
+  // which needs a positive scale (masked scores are -inf: a zero scale would
+  // turn them into NaN)
+  if (!std::isfinite(a->scale) || !(a->scale > 0.f)) return MLA_ERR_INVALID_ARG;
   if (a->profile_events && (!a->profile_events[0] || !a->profile_events[1])) return MLA_ERR_INVALID_ARG;
   return MLA_OK;
 }

@@ -93,6 +93,9 @@ def test_shape_validation(lib, field, value, status):
     ("page_size", 0, api.MLA_ERR_INVALID_ARG),
     ("kv_c", 0x10008, api.MLA_ERR_INVALID_ARG),         # not 16-byte aligned
     ("scale", float("nan"), api.MLA_ERR_INVALID_ARG),
+    ("scale", 0.0, api.MLA_ERR_INVALID_ARG),
+    ("scale", -0.07, api.MLA_ERR_INVALID_ARG),
+    ("scale", float("inf"), api.MLA_ERR_INVALID_ARG),
 ])
 def test_call_validation(lib, field, value, status):
     # the workspace size depends on shapes only; the call itself rejects these

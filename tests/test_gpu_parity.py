@@ -196,6 +196,18 @@ def test_padded_pool_rows(algo):
 
 
 @pytest.mark.parametrize("algo", ALGOS_BF16)
+@pytest.mark.parametrize("scale", [1.0, 1e-3], ids=["sharp", "flat"])
+def test_score_scales(algo, scale):
+    # scale 1 puts the scores' spread near 24 (a row's weights move the lazy
+    # running max tile after tile); scale 1e-3 makes the softmax nearly
+    # uniform over up to ~800 tokens
+    p = I.make_problem(name="scales", dtype="bf16", B=2, H=64, Q=16, prefix_lens=[300, 777], seed=32,
+                       layout="scattered", pool_slots=2048, scale=scale)
+    _, out, lse = run(p, algo=algo)
+    check_all_rows(p, out, lse, f"scale {scale}")
+
+
+@pytest.mark.parametrize("algo", ALGOS_BF16)
 def test_needles(algo):
     p = mid_problem(25)
     I.plant_needles(p, seed=5)
