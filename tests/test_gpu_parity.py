@@ -208,6 +208,27 @@ def test_score_scales(algo, scale):
 
 
 @pytest.mark.parametrize("algo", ALGOS_BF16)
+@pytest.mark.parametrize("num_splits", [1, 3, 0])
+def test_lse_may_be_null(algo, num_splits):
+    # lse is optional: with a NULL pointer the outputs are the same bytes
+    import ctypes
+    p = mid_problem(33)
+    di = api.device_inputs(p)
+    ref_out, _ = api.verify_attn(di, algo=algo, num_splits=num_splits)
+    out = torch.empty_like(ref_out)
+    a = api.make_args(di, out=out, lse=None, algo=algo)
+    assert not a.lse
+    lib = api.load()
+    n = lib.mla_verify_workspace_size(ctypes.byref(a), num_splits)
+    ws = api.alloc_workspace(n)
+    st = lib.mla_verify_attn(ctypes.byref(a), ctypes.c_void_p(ws.data_ptr()), ctypes.c_size_t(n), num_splits,
+                             api._stream(None))
+    assert st == api.MLA_OK
+    assert api.check(ws) == 0
+    assert torch.equal(out, ref_out)
+
+
+@pytest.mark.parametrize("algo", ALGOS_BF16)
 def test_needles(algo):
     p = mid_problem(25)
     I.plant_needles(p, seed=5)
