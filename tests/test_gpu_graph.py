@@ -97,3 +97,42 @@ def test_overlapped_launches_match_plain_launches(algo):
     assert api.check(ws) == 0
     for o, l in outs:
         assert torch.equal(o, ref_o) and torch.equal(l, ref_l)
+
+
+def test_graph_replay_follows_new_lengths():
+    # the split count is chosen on the device from prefix_lens, so a captured
+    # call re-plans when the caller shortens a sequence between replays (a
+    # plan fixed on the host at capture time could not)
+    p = I.make_problem(name="graph_len", dtype="bf16", B=1, H=64, Q=64, prefix_lens=[8000], seed=53,
+                       layout="scattered", pool_slots=9000)
+    di = api.device_inputs(p)
+    out = torch.empty((1, 64, 64, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((1, 64, 64), dtype=torch.float32, device="cuda")
+    ws = api.alloc_workspace(api.workspace_size(di, 0, algo="tc"))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        api.verify_attn(di, out=out, lse=lse, workspace=ws, algo="tc")
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        api.verify_attn(di, out=out, lse=lse, workspace=ws, algo="tc")
+    g.replay()
+    long_splits = api.splits_used(ws)
+
+    # 300 prefix tokens: the tree nodes now sit at positions 300..363 of the
+    # same index table
+    di.prefix_lens.fill_(300)
+    di.kv_indptr[1] = 300 + 64
+    g.replay()
+    short_splits = api.splits_used(ws)
+    assert api.check(ws) == 0
+    assert long_splits > short_splits >= 1, (long_splits, short_splits)
+    p.prefix_lens = np.array([300], dtype=np.int32)
+    p.kv_indptr = np.array([0, 364], dtype=np.int32)
+    rows = I.all_rows(p)
+    ro, rl = PT.oracle_rows(p, rows)
+    go, gl = PT.gather_rows(out, lse, rows)
+    PT.assert_close(go, ro, "bf16", "graph after shortening out")
+    PT.assert_close(gl, rl, "bf16", "graph after shortening lse")
