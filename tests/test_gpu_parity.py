@@ -228,6 +228,28 @@ def test_lse_may_be_null(algo, num_splits):
     assert torch.equal(out, ref_out)
 
 
+def test_two_streams_at_once():
+    # calls on two streams with their own workspaces share no device state:
+    # launched back to back without a synchronisation they give the bytes of
+    # the same calls made one after the other
+    probs = [mid_problem(34), ragged_batch_problem(35)]
+    dis = [api.device_inputs(p) for p in probs]
+    refs = [api.verify_attn(d, algo="tc") for d in dis]
+    torch.cuda.synchronize()
+    outs = [(torch.empty_like(o), torch.empty_like(l)) for o, l in refs]
+    wss = [api.alloc_workspace(api.workspace_size(d, 0, algo="tc")) for d in dis]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s_ in streams:
+        s_.wait_stream(torch.cuda.current_stream())
+    for _ in range(3):
+        for d, (o, l), w, s_ in zip(dis, outs, wss, streams):
+            api.verify_attn(d, out=o, lse=l, workspace=w, algo="tc", stream=s_)
+    torch.cuda.synchronize()
+    for (o, l), (ro, rl), w in zip(outs, refs, wss):
+        assert api.check(w) == 0
+        assert torch.equal(o, ro) and torch.equal(l, rl)
+
+
 @pytest.mark.parametrize("algo", ALGOS_BF16)
 def test_needles(algo):
     p = mid_problem(25)
