@@ -7,7 +7,8 @@
 // of the total exponent mass, is the softmax over the union.  When a call
 // keeps one chunk per row group the attention kernel writes the results
 // directly: this kernel is then not launched, or (the split count being chosen
-// on the device) returns at once.
+// on the device) returns at once -- unless the plan cut the items of a last,
+// partial wave into pieces, whose rows alone it then merges.
 #include "common.cuh"
 
 namespace mlav {
